@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Benchmark: DSA-layer forward+backward tokens/s on one GB300.
+
+Workload (default): the L=131072 bf16 layer with a 10% needle -- Hq=16 query
+heads sharing one K/V head of d=128, an indexer of 8 heads x 64, 32768 pools
+of 4 tokens, top-512 pools per query, indexer chunks of 8192 queries.
+Synthetic seeded inputs (dsa_inputs.py); no dataset, no trained weights.
+
+One step = the whole layer: pool keys, for each 8192-query chunk the indexer
+scores and the top-k, sparse attention forward, then the backward (dQ, dK,
+dV).  It calls the C-ABI entry points one by one on one stream, with CUDA
+events between them, so the per-kernel durations (and the roofline of the
+dominant kernel) are measured live in the same run.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, single thread, on this host's
+cores) on a bounded sample of the same workload: that is the only place the
+benchmark runs the oracle.  With N > 1 (torchrun), every rank runs an
+independent replica of the layer (the layer has no exchange step on one
+GPU); value = the sum over ranks of tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import dsa_inputs  # noqa: E402
+
+METRIC = "DSA-layer tokens/s fwd+bwd at L=128k on 1 GB300"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {k: float(j[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ algorithmic work
+def algorithmic(wl):
+    """Per-launch algorithmic bytes / flops of each kernel (causal, selected work only)."""
+    L, P, k, Hq, d, Hi, di = wl.L, wl.P, wl.k, wl.Hq, wl.d, wl.Hi, wl.di
+    t = torch.arange(L, dtype=torch.float64)
+    elig = torch.floor((t + 1) / 4)
+    pairs = float(elig.sum())
+    partial = torch.where(t % 4 == 3, 0.0, t % 4 + 1)
+    nkeys = float((4 * torch.minimum(elig, torch.tensor(float(k))) + partial).sum())
+    eb = 2 if wl.dtype == "bf16" else 4
+    return {
+        "pool_keys": {"bytes": L * di * eb + P * di * eb},
+        "indexer": {"flops": 2.0 * Hi * di * pairs, "score_bytes": 4.0 * pairs},
+        "topk": {"bytes": 4.0 * pairs + 4.0 * L * k},
+        "attn_fwd": {"bytes": nkeys * 2 * d * eb + L * Hq * d * eb * 2 + L * k * 4 + L * Hq * 4,
+                     "flops": 4.0 * Hq * d * nkeys},
+        "attn_bwd": {"bytes": nkeys * 2 * d * eb + nkeys * 2 * d * 4 + L * Hq * d * (3 * eb + 4) + L * k * 4,
+                     "flops": 10.0 * Hq * d * nkeys},
+        "nkeys": nkeys, "pairs": pairs,
+    }
+
+
+# -------------------------------------------------------------------- ours
+def run_ours(args, rank, world):
+    import long_context_sparse_dsa_gb300 as dsa
+    from long_context_sparse_dsa_gb300 import build as lib_build
+
+    wl = dsa_inputs.WORKLOADS[args.workload]
+    with_bwd = wl.passes == "fwd+bwd"
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(dsa.LIB_PATH):
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dsa.library()
+
+    names = ("Q", "K", "V", "q_I", "k_I", "w") + (("dO",) if with_bwd else ())
+    host = dsa_inputs.make(wl, names, pin=True)
+    d_in = {n: host[n].to(dev, non_blocking=True) for n in names}
+    dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
+    bufs = dsa.alloc_forward_buffers(dims, dev)
+    dq = torch.empty((wl.L, wl.Hq, wl.d), device=dev) if with_bwd else None
+    dk = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
+    dv = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
+    stream = torch.cuda.current_stream(dev)
+    scores = bufs.ws.view(torch.float32)
+    C = wl.q_chunk
+    chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
+    launches_per_step = 1 + 2 * len(chunks) + 1 + (1 if with_bwd else 0)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(timers=None):
+        marks = []
+        if timers is not None:
+            marks.append(("start", timers.pop()))
+            marks[-1][1].record(stream)
+        dsa.pool_keys(dims, d_in["k_I"], bufs.kpool, stream)
+        if timers is not None:
+            marks.append(("pool_keys", timers.pop()))
+            marks[-1][1].record(stream)
+        for q0, n in chunks:
+            dsa.indexer_score(dims, d_in["q_I"], bufs.kpool, d_in["w"], q0, n, scores, stream)
+            if timers is not None:
+                marks.append(("indexer", timers.pop()))
+                marks[-1][1].record(stream)
+            dsa.topk(dims, scores, q0, n, bufs.idx, stream)
+            if timers is not None:
+                marks.append(("topk", timers.pop()))
+                marks[-1][1].record(stream)
+        dsa.sparse_attn_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, stream)
+        if timers is not None:
+            marks.append(("attn_fwd", timers.pop()))
+            marks[-1][1].record(stream)
+        if with_bwd:
+            dsa.sparse_attn_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq,
+                                dk, dv, None, 0, stream)
+            if timers is not None:
+                marks.append(("attn_bwd", timers.pop()))
+                marks[-1][1].record(stream)
+        return marks
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    dsa.check_device_error(stream)
+
+    per_kernel = {}
+    step_ms = []
+    n_marks = 2 + 2 * len(chunks) + 2 + 1
+    with ClockSampler(local) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        for _ in range(args.steps):
+            flush.fill_(1)                                  # evict L2 between steps (outside the events)
+            timers = [ev() for _ in range(n_marks)]
+            marks = step(timers)
+            torch.cuda.synchronize(dev)
+            for (nm, e0), (nm1, e1) in zip(marks[:-1], marks[1:]):
+                per_kernel.setdefault(nm1, []).append(e0.elapsed_time(e1))
+            step_ms.append(marks[0][1].elapsed_time(marks[-1][1]))
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    dsa.check_device_error(stream)
+
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = wl.L * args.steps * world
+    value = tokens / (total_ms / 1e3)
+
+    # kernel totals per step (sum over chunk launches) and per-launch means
+    steps = args.steps
+    k_ms = {nm: sum(v) / steps for nm, v in per_kernel.items()}
+    launch_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
+    alg = algorithmic(wl)
+    peaks, peak_kind = load_peaks()
+    dominant = max(k_ms, key=k_ms.get)
+    rl = roofline(dominant, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))
+    kernels = {nm: {"ms_per_step": round(k_ms[nm], 4), "launches_per_step": len(per_kernel[nm]) // steps,
+                    **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))} for nm in k_ms}
+
+    # end-to-end through the C ABI with host buffers: H2D of the inputs, the layer, D2H of the results
+    e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_bwd, world, dev)
+    clocks = clk.summary()
+    return {
+        "metric": METRIC if args.workload == "bf16_128k_needle" else f"DSA-layer tokens/s ({wl.passes}) {wl.name}",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "L": wl.L, "Hq": wl.Hq, "d": wl.d, "Hi": wl.Hi, "di": wl.di, "k": wl.k,
+                   "q_chunk": wl.q_chunk, "pass": wl.passes, "needle": wl.needle,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MiB buffer written before every timed step, outside the events"},
+        "roofline": rl,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+
+
+def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks):
+    ms = launch_ms[nm]
+    hbm = peaks["hbm_gbs"]
+    if nm == "indexer":
+        flops = alg["indexer"]["flops"] / nchunks      # one launch = one chunk (average)
+        a = flops / (ms * 1e-3) / 1e12
+        pk = peaks["bf16_tflops"]
+        return {"bound": "tensor", "achieved": round(a, 2), "peak": pk, "unit": "TFLOP/s", "frac": round(a / pk, 4),
+                "traffic": None, "peak_source": f"{peak_kind} bf16 dense (burst)"}
+    if nm == "topk":
+        b = alg["topk"]["bytes"] / nchunks
+    elif nm == "pool_keys":
+        b = alg["pool_keys"]["bytes"]
+    else:
+        b = alg[nm]["bytes"]
+    a = b / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+            "traffic": None, "peak_source": f"{peak_kind} HBM copy"}
+
+
+def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_bwd, world, dev):
+    names = list(d_in.keys())
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
+    pinned_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    steps = max(1, min(args.steps, 3))
+
+    def one():
+        for n in names:
+            d_in[n].copy_(host[n], non_blocking=True)
+        dsa.layer_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], d_in["q_I"], d_in["k_I"], d_in["w"], bufs.o, bufs.lse,
+                      bufs.idx, bufs.kpool, bufs.ws, stream=stream)
+        if with_bwd:
+            dsa.layer_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq, dk, dv,
+                          stream=stream)
+        for src, dst in zip(outs, pinned_out):
+            dst.copy_(src, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(wl.L * steps * world / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_sample(wl, n_rows: int, seed: int = 7):
+    """Time the CPU oracle (single thread) on n_rows query rows of the workload:
+    pool keys, the rows' indexer scores and top-k, their attention forward and
+    backward.  Returns (seconds, rows, description)."""
+    import numpy as np
+    import oracle
+
+    oracle.build()
+    with_bwd = wl.passes == "fwd+bwd"
+    names = ("Q", "K", "V", "q_I", "k_I", "w") + (("dO",) if with_bwd else ())
+    host = dsa_inputs.make(wl, names)
+    g = torch.Generator().manual_seed(seed)
+    rows = np.sort(torch.randint(wl.L // 2, wl.L, (n_rows,), generator=g).numpy()).astype(np.int64)
+    f = {n: host[n].to(torch.float32).numpy() for n in ("K", "V", "q_I", "k_I", "w")}
+    Qr = host["Q"][rows].to(torch.float32).numpy()
+    dOr = host["dO"][rows].to(torch.float32).numpy() if with_bwd else None
+    t0 = time.perf_counter()
+    kp = oracle.pool_keys(f["k_I"], wl.dtype == "bf16")
+    t_pool = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    sc = oracle.indexer_scores(f["q_I"], kp, f["w"], rows)
+    sel = oracle.topk(sc, wl.L, wl.k, rows)
+    idx = np.full((wl.L, wl.k), -1, np.int32)
+    idx[rows] = sel
+    oracle.attn_fwd(Qr, f["K"], f["V"], idx, wl.scale, rows, q_compact=True)
+    if with_bwd:
+        oracle.attn_bwd(Qr, f["K"], f["V"], idx, dOr, wl.scale, rows, with_dkv=True, threads=1, q_compact=True)
+    t_rows = time.perf_counter() - t1
+    # the pool-key pass is per layer: charge it in proportion to the rows sampled
+    secs = t_rows + t_pool * (n_rows / wl.L)
+    desc = (f"{n_rows} query rows drawn uniformly from the second half of the sequence: indexer scores over all "
+            f"eligible pools, top-{wl.k}, attention {wl.passes} with dK/dV; pool keys once, charged per row")
+    return secs, n_rows, desc
+
+
+def run_reference(args):
+    wl = dsa_inputs.WORKLOADS[args.workload]
+    per_step_rows = max(1, args.ref_rows)
+    times = []
+    for s in range(args.warmup + args.steps):
+        secs, n, desc = oracle_sample(wl, per_step_rows, seed=100 + s)
+        if s >= args.warmup:
+            times.append(secs)
+    total = sum(times)
+    value = per_step_rows * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC if args.workload == "bf16_128k_needle" else wl.name,
+        "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "L": wl.L, "k": wl.k, "pass": wl.passes},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="bf16_128k_needle", choices=sorted(dsa_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per reference step")
+    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for the cpu_baseline field")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            wl = dsa_inputs.WORKLOADS[args.workload]
+            secs, n, desc = oracle_sample(wl, args.cpu_rows)
+            line["cpu_baseline"] = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                    "sample": desc, "seconds": round(secs, 2)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek Sparse Attention layer library
+ * (libdsa_gb300.so).
+ *
+ * One DSA layer: a lightning indexer scores every causal 4-token key pool for
+ * every query, a per-query top-k keeps the best pools, and attention runs
+ * only over the tokens of those pools (plus the query's own partial pool).
+ *
+ * Source passages (page "SkyRL extends GLM-5.3-Flash training context to 1
+ * million tokens"):
+ *   section "Model and bottleneck": the indexer scores one pool per 4 tokens
+ *     for every query; attention then reads about 2048 keys per query;
+ *   section "1. DSA truly sparse": no positional encoding (NoPE); 2051 keys
+ *     rather than 2048; the indexer is scored in query chunks; selected pool
+ *     indices are int32; a kernel that silently rejects a shape and falls back
+ *     to dense attention is the failure to avoid.
+ * The pages print no formula; the definitions below are the plainest reading
+ * of those passages:
+ *   elig(t)      = floor((t+1)/4)   pools whose 4 tokens are all <= t
+ *   kpool[p]     = k_I[4p] + k_I[4p+1] + k_I[4p+2] + k_I[4p+3]
+ *                  (fp32 adds in that order, rounded once to the layer dtype)
+ *   s[t,p]       = sum_h w[t,h] * max(0, q_I[t,h,:] . kpool[p,:]),  p < elig(t)
+ *   idx[t,:]     = the min(k, elig(t)) best pools by (score desc, pool asc),
+ *                  listed in ascending pool order, padded with -1
+ *   keys(t)      = tokens of idx[t,:], plus 4*floor(t/4) .. t when t%4 != 3
+ *   O[t,h]       = softmax_j(scale * Q[t,h] . K[j]) V[j] over j in keys(t)
+ *   LSE[t,h]     = log sum_j exp(scale * Q[t,h] . K[j])  (natural log)
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
+ *     by the caller.  The library never allocates, frees or synchronises
+ *     device memory or streams, except dsa_check_device_error (which
+ *     synchronises the given stream).
+ *   - Work is enqueued on `stream` and runs asynchronously; a DSA_OK return
+ *     means the launches were accepted, not that they finished.
+ *   - Arguments are validated before anything is launched.  A shape the
+ *     kernels do not support returns DSA_ERR_UNSUPPORTED: there is no
+ *     fallback to another algorithm, dense or otherwise.
+ *   - Every pointer must be 16-byte aligned.
+ *   - Layer-dtype tensors (Q, K, V, q_I, k_I, kpool, O, dO) are fp32 or bf16
+ *     per dims->dtype; w, scores, LSE, dQ, dK, dV are fp32; idx is int32.
+ *   - Kernels never trap.  A bad index inside idx (a pool the query may not
+ *     see) is skipped and recorded in a device error word, read back by
+ *     dsa_check_device_error.
+ *   - Results of the forward steps (pool keys, scores, top-k, attention
+ *     forward) are bitwise reproducible run to run.  The backward adds dK/dV
+ *     contributions with fp32 atomics, so its summation order varies.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dsa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad range, L % 4 != 0, k < 1, ... */
+    DSA_ERR_UNSUPPORTED = 2,  /* a shape or dtype the kernels do not implement */
+    DSA_ERR_WORKSPACE = 3,    /* workspace pointer missing or smaller than required */
+    DSA_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed */
+    DSA_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (see dsa_check_device_error) */
+    DSA_ERR_BAD_INDEX = 6     /* idx named a pool outside 0..elig(t)-1 (entry skipped) */
+} dsa_status;
+
+typedef enum { DSA_FP32 = 0, DSA_BF16 = 1 } dsa_dtype;
+
+/* Layer shape, passed by pointer to every entry point.
+ *   L       tokens; a multiple of 4 (pool size), >= 4
+ *   Hq      query heads sharing the single K/V head
+ *   d       attention head dim
+ *   Hi      indexer heads
+ *   di      indexer head dim
+ *   pool    tokens per pool; must be 4
+ *   k       pools kept per query, >= 1
+ *   q_chunk queries scored per indexer chunk inside dsa_layer_fwd (bounds the
+ *           score workspace to q_chunk * (L/4) fp32 values); >= 1
+ *   scale   softmax scale (1/sqrt(d) for the usual layer)
+ *   dtype   dsa_dtype of the layer-dtype tensors
+ * Supported shapes (anything else -> DSA_ERR_UNSUPPORTED):
+ *   bf16: d in {64,128}, Hq in {16,32}, di in {64,128}, Hi in {4,8}, k <= 1024
+ *   fp32: d in {64,128}, 1 <= Hq <= 32, di in {64,128}, 1 <= Hi <= 8, k <= 1024
+ *         (backward is bf16 only)
+ */
+typedef struct dsa_dims {
+    int64_t L;
+    int32_t Hq;
+    int32_t d;
+    int32_t Hi;
+    int32_t di;
+    int32_t pool;
+    int32_t k;
+    int32_t q_chunk;
+    float scale;
+    int32_t dtype;
+} dsa_dims;
+
+/* Short English name of a status code (static storage). */
+const char *dsa_status_string(dsa_status status);
+
+/* Detail of the last non-OK status returned on the calling host thread
+ * (static thread-local storage; empty string if none). */
+const char *dsa_last_error_message(void);
+
+/* Validate `dims` for the given pass (0 = forward, 1 = forward+backward)
+ * without touching the GPU.  Returns DSA_OK, DSA_ERR_INVALID_ARG or
+ * DSA_ERR_UNSUPPORTED. */
+dsa_status dsa_validate_dims(const dsa_dims *dims, int32_t with_backward);
+
+/* Bytes of device workspace dsa_layer_fwd needs: the fp32 score block of one
+ * query chunk, q_chunk * (L/4) * 4 bytes, rounded up to 256.  Returns 0 if
+ * dims are invalid.  dsa_layer_bwd and dsa_sparse_attn_bwd need none. */
+size_t dsa_workspace_bytes(const dsa_dims *dims);
+
+/* Pool keys.  Page "SkyRL extends GLM-5.3-Flash ...", section "Model and
+ * bottleneck" (one pool per 4 tokens).
+ *   k_idx  [L, di]     layer dtype, the indexer's per-token keys k_I
+ *   kpool  [L/4, di]   layer dtype, output: kpool[p] as defined above
+ * Bitwise equal to the definition (fp32 sum in token order, one rounding). */
+dsa_status dsa_pool_keys(const dsa_dims *dims, const void *k_idx, void *kpool, dsa_stream_t stream);
+
+/* Indexer scores for queries q_begin .. q_begin+q_count-1.  Same page,
+ * sections "Model and bottleneck" and "1. DSA truly sparse" (chunked by
+ * query).  bf16 runs on the tcgen05 tensor cores (fp32 accumulation in
+ * tensor memory, ReLU and the weighted head sum fused into the epilogue).
+ *   q_idx   [L, Hi, di] layer dtype, indexer queries q_I
+ *   kpool   [L/4, di]   layer dtype, from dsa_pool_keys
+ *   w       [L, Hi]     fp32 head weights
+ *   scores  [q_count, L/4] fp32, output; row r is query q_begin+r.  Only
+ *           entries p < elig(q_begin+r) are written; the rest are untouched.
+ * Requires 0 <= q_begin, q_count >= 1, q_begin+q_count <= L. */
+dsa_status dsa_indexer_score(const dsa_dims *dims, const void *q_idx, const void *kpool, const float *w,
+                             int64_t q_begin, int64_t q_count, float *scores, dsa_stream_t stream);
+
+/* Per-query top-k pool selection.  Same page, "Model and bottleneck" (about
+ * 2048 keys = 512 pools per query) and "1. DSA truly sparse" (int32 pool
+ * indices).  Radix select over the fp32 score bits; -0 and +0 tie; ties go
+ * to the lower pool index; only p < elig(t) is considered (causality).
+ *   scores  [q_count, L/4] fp32 as written by dsa_indexer_score for the same
+ *           q_begin/q_count
+ *   idx     [L, k] int32; rows q_begin .. q_begin+q_count-1 are written:
+ *           selected pools in ascending order, then -1 padding. */
+dsa_status dsa_topk(const dsa_dims *dims, const float *scores, int64_t q_begin, int64_t q_count,
+                    int32_t *idx, dsa_stream_t stream);
+
+/* Sparse attention forward over keys(t).  Same page, "1. DSA truly sparse"
+ * (sparse kernel, NoPE, 2051 keys).  One K/V head shared by all Hq heads.
+ *   q    [L, Hq, d]  layer dtype        k, v [L, d] layer dtype
+ *   idx  [L, k]      int32 (from dsa_topk or the caller; entries < 0 skipped)
+ *   o    [L, Hq, d]  layer dtype, output
+ *   lse  [L, Hq]     fp32, output (natural log) */
+dsa_status dsa_sparse_attn_fwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                               const int32_t *idx, void *o, float *lse, dsa_stream_t stream);
+
+/* Sparse attention backward (bf16 only).  Given dO, writes
+ *   dq [L, Hq, d] fp32 (overwritten), dk, dv [L, d] fp32 (zeroed on the
+ *   stream, then accumulated with fp32 atomics).
+ * o and lse must be the forward's outputs for the same q, k, v, idx.  The
+ * selection is piecewise constant: no gradient reaches the indexer inputs.
+ * ws/ws_bytes are accepted for ABI stability and may be NULL/0. */
+dsa_status dsa_sparse_attn_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                               const int32_t *idx, const void *o, const float *lse, const void *dout,
+                               float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                               dsa_stream_t stream);
+
+/* Whole forward: dsa_pool_keys once, then per chunk of q_chunk queries
+ * dsa_indexer_score -> dsa_topk into the workspace, then dsa_sparse_attn_fwd.
+ *   outputs: o [L,Hq,d], lse [L,Hq], idx [L,k], kpool [L/4,di]
+ *   ws      >= dsa_workspace_bytes(dims) bytes of device memory */
+dsa_status dsa_layer_fwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                         const void *q_idx, const void *k_idx, const float *w,
+                         void *o, float *lse, int32_t *idx, void *kpool,
+                         void *ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Whole backward: dsa_sparse_attn_bwd with the idx and lse the forward
+ * saved (the indexer is not recomputed and gets no gradient). */
+dsa_status dsa_layer_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                         const int32_t *idx, const void *o, const float *lse, const void *dout,
+                         float *dq, float *dk, float *dv, void *ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word that the
+ * kernels set instead of trapping.  Returns DSA_OK, DSA_ERR_TIMEOUT (a
+ * bounded wait gave up; the kernel freed its resources and returned),
+ * DSA_ERR_BAD_INDEX, or DSA_ERR_CUDA if the synchronisation itself failed. */
+dsa_status dsa_check_device_error(dsa_stream_t stream);
+
+/* Test hook: the number of spin iterations after which a bounded device-side
+ * wait gives up (default 1<<20, about a second at most).  Lowering it lets a test make a wait run
+ * out.  Takes effect for launches enqueued after the call. */
+void dsa_set_wait_limit(uint32_t spins);
+
+/* Test hook for the failure-detection path: enqueue a one-CTA kernel that
+ * waits on an mbarrier nothing arrives on.  The bounded wait gives up after
+ * `spins` polls (1 .. 2^24) and records a timeout; the kernel then returns
+ * normally and the stream stays usable.  dsa_check_device_error(stream)
+ * afterwards returns DSA_ERR_TIMEOUT. */
+dsa_status dsa_selftest_bounded_wait(uint32_t spins, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_GB300_H */

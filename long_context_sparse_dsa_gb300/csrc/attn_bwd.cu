@@ -1,0 +1,355 @@
+// attn_bwd.cu -- sparse attention backward (bf16 inputs, fp32 gradients).
+//
+// Page "SkyRL extends GLM-5.3-Flash training context to 1 million tokens",
+// section "1. DSA truly sparse" (the sparse kernel runs forward and backward)
+// and section "2. Activation recomputation and offload" (the layer is
+// recomputed from saved inputs, which is why only idx and LSE are kept).
+//
+// For query t, head h, key j in keys(t) (as in the forward):
+//   P = exp(scale*Q.K[j] - LSE),  D = dO . O,  dP = dO . V[j],
+//   dS = P (dP - D),  dQ = scale sum_j dS K[j],
+//   dK[j] += scale sum_h dS Q[t,h],  dV[j] += sum_h P dO[t,h].
+// The selection is piecewise constant, so q_I, k_I and w get no gradient.
+//
+// One warp per (query, 16-head group), the same 16-key gather pipeline as
+// the forward.  dQ stays in registers for the whole query.  Per 16-key step
+// the warp computes the 16x16 S and dP tiles with m16n8k16 MMAs (heads on M),
+// then the 16-key x d tiles of dK and dV with the keys on M: the transposed
+// P and dS operands are built in registers with movmatrix, and Q / dO come
+// from a per-warp swizzled shared copy.  The dK/dV products run in fp16
+// (P, scale*dS, Q, dO converted; 10-bit mantissa instead of bf16's 7) because
+// those sums collect contributions from every query that selected a key.  Each finished dK/dV fragment goes to
+// global memory with fp32 vector reductions (red.global.add.v2.f32), so the
+// summation order across queries is not fixed.
+#include "common.cuh"
+#include "launch.h"
+
+namespace dsa {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KEYS = 16;
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int CHUNKS = D / 8;
+  static constexpr int TILE_BYTES = KEYS * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int WARPS = 4;
+  static constexpr int WARP_BYTES = NST * STAGE_BYTES + 2 * TILE_BYTES;  // stages + Q + dO copies
+  static constexpr int SMEM = WARPS * WARP_BYTES;
+  static constexpr int COPIES = 2 * KEYS * CHUNKS / 32;
+};
+
+__device__ __forceinline__ int64_t bwd_slot_pool(const int32_t* irow, int k, int slot, int64_t t) {
+  if (slot < k) {
+    const int64_t p = __ldg(irow + slot);
+    if (p < 0) return -1;
+    if (p >= elig(t)) {
+      record_error(DSA_DEV_ERR_BAD_INDEX);
+      return -1;
+    }
+    return p;
+  }
+  if (slot == k && (t & 3) != 3) return t >> 2;
+  return -1;
+}
+
+// Eight bf16 values -> eight fp16 values (exact for |x| in [2^-14, 65504]).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    out[i] = pack_f16(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_gather(uint32_t stage, const __nv_bfloat16* __restrict__ K,
+                                           const __nv_bfloat16* __restrict__ V, int64_t my_pool, int lane,
+                                           int64_t t, int k, int group) {
+  using C = BwdCfg<D>;
+#pragma unroll
+  for (int i = 0; i < C::COPIES; ++i) {
+    const int cid = i * 32 + lane;
+    const int sig = cid / (8 * C::CHUNKS);
+    const int rem = cid % (8 * C::CHUNKS);
+    const int tensor = rem / (4 * C::CHUNKS);
+    const int rr = rem % (4 * C::CHUNKS);
+    const int row = rr / C::CHUNKS;
+    const int ch = rr % C::CHUNKS;
+    const int64_t p = __shfl_sync(0xffffffffu, my_pool, sig);
+    const int slot = group * 4 + sig;
+    const int64_t tok = 4 * p + row;
+    const bool valid = p >= 0 && (slot != k || tok <= t);
+    const __nv_bfloat16* src = (tensor ? V : K) + (valid ? tok * D + ch * 8 : 0);
+    const int key = sig * 4 + row;
+    cp_async16(stage + tensor * C::TILE_BYTES + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), src,
+               valid ? 16u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
+    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
+    const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
+    const __nv_bfloat16* __restrict__ dO, float* __restrict__ dQ, float* __restrict__ dK, float* __restrict__ dV,
+    int64_t L, int Hq, int k, float scale, float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(128) unsigned char bwd_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HG = Hq / 16;
+  const int64_t items = L * HG;
+  const int64_t item = items - 1 - ((int64_t)blockIdx.x * C::WARPS + warp);
+  if (item < 0) return;
+  const int64_t t = item / HG;
+  const int hg = (int)(item % HG);
+  const uint32_t wbase = smem_u32(bwd_smem) + warp * C::WARP_BYTES;
+  const uint32_t qs = wbase + C::NST * C::STAGE_BYTES;
+  const uint32_t dos = qs + C::TILE_BYTES;
+  const int32_t* irow = idx + t * k;
+  const int nslots = k + 1;
+  const int ngroups = (nslots + 3) / 4;
+  const int g = lane >> 2, qi = lane & 3;
+  const int64_t row0 = t * Hq + hg * 16;  // first (t, head) row of this warp
+
+  // Per-warp swizzled fp16 copies of Q and dO (16 heads x D), 16-byte chunks;
+  // the B operands of the dK and dV products.
+  {
+    const uint4* q4 = reinterpret_cast<const uint4*>(Q + row0 * D);
+    const uint4* d4 = reinterpret_cast<const uint4*>(dO + row0 * D);
+    unsigned char* qsp = bwd_smem + (qs - smem_u32(bwd_smem));
+    unsigned char* dsp = bwd_smem + (dos - smem_u32(bwd_smem));
+    for (int c = lane; c < 16 * C::CHUNKS; c += 32) {
+      const int r = c / C::CHUNKS, ch = c % C::CHUNKS;
+      const int off = r * C::ROW_BYTES + ((ch ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(qsp + off) = bf16x8_to_f16x8(__ldg(q4 + c));
+      *reinterpret_cast<uint4*>(dsp + off) = bf16x8_to_f16x8(__ldg(d4 + c));
+    }
+  }
+  // D[h] = dO[h] . O[h] for the 16 heads: lane pair (2h, 2h+1) splits row h.
+  float Dg, Dg8;
+  {
+    const int h = lane >> 1, half = lane & 1;
+    const uint4* o4 = reinterpret_cast<const uint4*>(O + (row0 + h) * D) + half * (C::CHUNKS / 2);
+    const uint4* d4 = reinterpret_cast<const uint4*>(dO + (row0 + h) * D) + half * (C::CHUNKS / 2);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < C::CHUNKS / 2; ++c) {
+      const uint4 a = __ldg(o4 + c), b = __ldg(d4 + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    Dg = __shfl_sync(0xffffffffu, acc, 2 * g);
+    Dg8 = __shfl_sync(0xffffffffu, acc, 2 * (g + 8));
+  }
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float lse_g = __ldg(LSE + row0 + g) * kLog2e;
+  const float lse_g8 = __ldg(LSE + row0 + g + 8) * kLog2e;
+  __syncwarp();
+
+  // A fragments of Q and dO (rows = heads), bf16, straight from global memory.
+  uint32_t qa[D / 16][4], da[D / 16][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(Q + row0 * D);
+    const uint32_t* d32 = reinterpret_cast<const uint32_t*>(dO + row0 * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int c0 = (g * D + ks * 16 + 2 * qi) / 2, c1 = ((g + 8) * D + ks * 16 + 2 * qi) / 2;
+      qa[ks][0] = __ldg(q32 + c0);
+      qa[ks][1] = __ldg(q32 + c1);
+      qa[ks][2] = __ldg(q32 + c0 + 4);
+      qa[ks][3] = __ldg(q32 + c1 + 4);
+      da[ks][0] = __ldg(d32 + c0);
+      da[ks][1] = __ldg(d32 + c1);
+      da[ks][2] = __ldg(d32 + c0 + 4);
+      da[ks][3] = __ldg(d32 + c1 + 4);
+    }
+  }
+
+  float dq[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) dq[n][0] = dq[n][1] = dq[n][2] = dq[n][3] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < C::NST - 1; ++s) {
+    if (s < ngroups) {
+      const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, s * 4 + lane, t) : -1;
+      bwd_gather<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, s);
+    }
+    cp_async_commit();
+  }
+
+  for (int grp = 0; grp < ngroups; ++grp) {
+    {
+      const int nx = grp + C::NST - 1;
+      if (nx < ngroups) {
+        const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, nx * 4 + lane, t) : -1;
+        bwd_gather<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, nx);
+      }
+      cp_async_commit();
+    }
+    const int64_t cur = lane < 4 ? bwd_slot_pool(irow, k, grp * 4 + lane, t) : -1;
+    // validity of this lane's S/dP columns (keys nt*8 + 2qi + e)
+    bool kv[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int sig = nt * 2 + (qi >> 1);
+      const int64_t p = __shfl_sync(0xffffffffu, cur, sig);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) kv[nt][e] = p >= 0 && (grp * 4 + sig != k || 4 * p + 2 * (qi & 1) + e <= t);
+    }
+    // tokens of the dK/dV fragment rows this lane adds into: keys g and g+8
+    int64_t tok_lo, tok_hi;
+    {
+      const int64_t p_lo = __shfl_sync(0xffffffffu, cur, g >> 2);
+      const int64_t p_hi = __shfl_sync(0xffffffffu, cur, 2 + (g >> 2));
+      tok_lo = 4 * p_lo + (g & 3);
+      tok_hi = 4 * p_hi + (g & 3);
+      if (p_lo < 0 || (grp * 4 + (g >> 2) == k && tok_lo > t)) tok_lo = -1;
+      if (p_hi < 0 || (grp * 4 + 2 + (g >> 2) == k && tok_hi > t)) tok_hi = -1;
+    }
+    cp_async_wait<C::NST - 1>();
+    __syncwarp();
+    const uint32_t ks_base = wbase + (grp % C::NST) * C::STAGE_BYTES;
+    const uint32_t vs_base = ks_base + C::TILE_BYTES;
+
+    // S = Q K^T and dP = dO V^T (heads x 16 keys)
+    float s[2][4], dp[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = dp[nt][e] = 0.f;
+    {
+      const int mtx = lane >> 3, r = lane & 7;
+      const int key = (mtx >> 1) * 8 + r;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int ch = 2 * ks + (mtx & 1);
+        const uint32_t off = key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ks_base + off, b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        ldsm_x4(vs_base + off, b0, b1, b2, b3);
+        mma_bf16_16816(dp[0], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b0, b1);
+        mma_bf16_16816(dp[1], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b2, b3);
+      }
+    }
+    // P and scale*dS: bf16 for the dQ product, fp16 for dK/dV (rows g: elements 0,1; rows g+8: 2,3)
+    uint32_t pp[2][2], dd[2][2], dh[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float p0 = kv[nt][0] ? exp2f(s[nt][0] * scale_log2 - lse_g) : 0.f;
+      const float p1 = kv[nt][1] ? exp2f(s[nt][1] * scale_log2 - lse_g) : 0.f;
+      const float p2 = kv[nt][0] ? exp2f(s[nt][2] * scale_log2 - lse_g8) : 0.f;
+      const float p3 = kv[nt][1] ? exp2f(s[nt][3] * scale_log2 - lse_g8) : 0.f;
+      const float s0 = scale * p0 * (dp[nt][0] - Dg), s1 = scale * p1 * (dp[nt][1] - Dg);
+      const float s2 = scale * p2 * (dp[nt][2] - Dg8), s3 = scale * p3 * (dp[nt][3] - Dg8);
+      pp[nt][0] = pack_f16(p0, p1);
+      pp[nt][1] = pack_f16(p2, p3);
+      dd[nt][0] = pack_bf16(s0, s1);
+      dd[nt][1] = pack_bf16(s2, s3);
+      dh[nt][0] = pack_f16(s0, s1);
+      dh[nt][1] = pack_f16(s2, s3);
+    }
+    // dQ += scale*dS K   (A = dS rows=heads, B = K^T via transposed loads)
+    {
+      const int mtx = lane >> 3, r = lane & 7;
+      const int key = (mtx & 1) * 8 + r;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int ch = 2 * j + (mtx >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(ks_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(dq[2 * j], dd[0][0], dd[0][1], dd[1][0], dd[1][1], b0, b1);
+        mma_bf16_16816(dq[2 * j + 1], dd[0][0], dd[0][1], dd[1][0], dd[1][1], b2, b3);
+      }
+    }
+    // dV[keys] += P^T dO and dK[keys] += (scale*dS)^T Q   (rows = keys)
+    const uint32_t pt0 = movmatrix_t(pp[0][0]), pt1 = movmatrix_t(pp[1][0]);
+    const uint32_t pt2 = movmatrix_t(pp[0][1]), pt3 = movmatrix_t(pp[1][1]);
+    const uint32_t dt0 = movmatrix_t(dh[0][0]), dt1 = movmatrix_t(dh[1][0]);
+    const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
+    {
+      const int mtx = lane >> 3, r = lane & 7;
+      const int hrow = (mtx & 1) * 8 + r;
+      float* dv_lo = tok_lo >= 0 ? dV + tok_lo * D + 2 * qi : nullptr;
+      float* dv_hi = tok_hi >= 0 ? dV + tok_hi * D + 2 * qi : nullptr;
+      float* dk_lo = tok_lo >= 0 ? dK + tok_lo * D + 2 * qi : nullptr;
+      float* dk_hi = tok_hi >= 0 ? dK + tok_hi * D + 2 * qi : nullptr;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int ch = 2 * j + (mtx >> 1);
+        const uint32_t off = hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        float cv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ldsm_x4_t(dos + off, b0, b1, b2, b3);
+        mma_f16_16816(cv[0], pt0, pt1, pt2, pt3, b0, b1);
+        mma_f16_16816(cv[1], pt0, pt1, pt2, pt3, b2, b3);
+        float ck[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ldsm_x4_t(qs + off, b0, b1, b2, b3);
+        mma_f16_16816(ck[0], dt0, dt1, dt2, dt3, b0, b1);
+        mma_f16_16816(ck[1], dt0, dt1, dt2, dt3, b2, b3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = (2 * j + h) * 8;
+          if (dv_lo) {
+            red_add_v2(dv_lo + col, cv[h][0], cv[h][1]);
+            red_add_v2(dk_lo + col, ck[h][0], ck[h][1]);
+          }
+          if (dv_hi) {
+            red_add_v2(dv_hi + col, cv[h][2], cv[h][3]);
+            red_add_v2(dk_hi + col, ck[h][2], ck[h][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  float* q0 = dQ + (row0 + g) * D + 2 * qi;
+  float* q8 = q0 + 8 * D;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    *reinterpret_cast<float2*>(q0 + n * 8) = make_float2(dq[n][0], dq[n][1]);
+    *reinterpret_cast<float2*>(q8 + n * 8) = make_float2(dq[n][2], dq[n][3]);
+  }
+}
+
+cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                 const void* v, const int32_t* idx, const void* o, const float* lse,
+                                 const void* dout, float* dq, float* dk, float* dv, cudaStream_t s) {
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const int64_t items = L * (Hq / 16);
+  const int64_t blocks = (items + 3) / 4;
+  auto qp = static_cast<const __nv_bfloat16*>(q);
+  auto kp = static_cast<const __nv_bfloat16*>(kk);
+  auto vp = static_cast<const __nv_bfloat16*>(v);
+  auto op = static_cast<const __nv_bfloat16*>(o);
+  auto gp = static_cast<const __nv_bfloat16*>(dout);
+  if (d == 128) {
+    constexpr int smem = BwdCfg<128>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_bwd_bf16_kernel<128><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, gp, dq, dk, dv, L, Hq,
+                                                                  k, scale, scale_log2);
+  } else if (d == 64) {
+    constexpr int smem = BwdCfg<64>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_bwd_bf16_kernel<64><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, gp, dq, dk, dv, L, Hq,
+                                                                 k, scale, scale_log2);
+  } else {
+    return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

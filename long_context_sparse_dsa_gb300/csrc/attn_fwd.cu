@@ -1,0 +1,379 @@
+// attn_fwd.cu -- sparse attention forward over the selected pools.
+//
+// Page "SkyRL extends GLM-5.3-Flash training context to 1 million tokens",
+// section "Model and bottleneck" (about 2048 keys read per query, so the
+// attention itself is close to linear in L) and section "1. DSA truly sparse"
+// (a truly sparse kernel; no positional encoding; 2051 = 4*512+3 keys).
+//
+// Keys of query t: the tokens of the pools in idx[t,:] (entries < 0 skipped),
+// then the query's own partial pool 4*floor(t/4) .. t when t%4 != 3.
+// O[t,h] = softmax(scale * Q[t,h] . K[keys]) V[keys]; LSE in natural log.
+//
+// bf16 kernel: one warp per (query, 16-head group).  A pool's 4 K rows (and
+// 4 V rows) are one contiguous 1 KB block, so the warp gathers 4 pools = 16
+// keys per step with 16-byte cp.async copies into an XOR-swizzled shared
+// tile (3-stage ring per warp, no CTA-wide barriers).  The 16 heads of one
+// query share every gathered key, which makes heads the M=16 side of
+// m16n8k16 bf16 MMAs: S = Q K^T and O += P V, fp32 accumulation, online
+// softmax in registers.  The kernel is bound by the L2->SM gather bandwidth
+// (about 16 flop per gathered byte), not by the MMAs.
+#include "common.cuh"
+#include "launch.h"
+
+namespace dsa {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int KEYS = 16;                    // keys per step (4 pool slots)
+  static constexpr int ROW_BYTES = D * 2;
+  static constexpr int CHUNKS = D / 8;               // 16-byte chunks per row
+  static constexpr int TILE_BYTES = KEYS * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
+  static constexpr int NST = 3;
+  static constexpr int WARPS = 4;
+  static constexpr int SMEM = WARPS * NST * STAGE_BYTES;
+  static constexpr int COPIES = 2 * KEYS * CHUNKS / 32;  // 16-byte copies per lane per step
+};
+
+// Pool of slot `slot` for query t, or -1 if the slot holds no visible pool.
+// Slot k is the query's own partial pool.  Bad indices are recorded and skipped.
+__device__ __forceinline__ int64_t slot_pool(const int32_t* irow, int k, int slot, int64_t t) {
+  if (slot < k) {
+    const int64_t p = __ldg(irow + slot);
+    if (p < 0) return -1;
+    if (p >= elig(t)) {
+      record_error(DSA_DEV_ERR_BAD_INDEX);
+      return -1;
+    }
+    return p;
+  }
+  if (slot == k && (t & 3) != 3) return t >> 2;
+  return -1;
+}
+
+template <int D>
+__device__ __forceinline__ void gather_step(uint32_t stage, const __nv_bfloat16* __restrict__ K,
+                                            const __nv_bfloat16* __restrict__ V, int64_t my_pool, int lane,
+                                            int64_t t, int k, int group) {
+  using C = FwdCfg<D>;
+#pragma unroll
+  for (int i = 0; i < C::COPIES; ++i) {
+    const int cid = i * 32 + lane;
+    const int sig = cid / (8 * C::CHUNKS);           // slot within the step
+    const int rem = cid % (8 * C::CHUNKS);
+    const int tensor = rem / (4 * C::CHUNKS);         // 0 = K, 1 = V
+    const int rr = rem % (4 * C::CHUNKS);
+    const int row = rr / C::CHUNKS;
+    const int ch = rr % C::CHUNKS;
+    const int64_t p = __shfl_sync(0xffffffffu, my_pool, sig);
+    const int slot = group * 4 + sig;
+    const int64_t tok = 4 * p + row;
+    const bool valid = p >= 0 && (slot != k || tok <= t);
+    const __nv_bfloat16* base = tensor ? V : K;
+    const __nv_bfloat16* src = base + (valid ? tok * D + ch * 8 : 0);
+    const int key = sig * 4 + row;
+    const uint32_t dst = stage + tensor * C::TILE_BYTES + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4);
+    cp_async16(dst, src, valid ? 16u : 0u);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                            const __nv_bfloat16* __restrict__ K,
+                                                            const __nv_bfloat16* __restrict__ V,
+                                                            const int32_t* __restrict__ idx,
+                                                            __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
+                                                            int64_t L, int Hq, int k, float scale_log2) {
+  using C = FwdCfg<D>;
+  extern __shared__ __align__(128) unsigned char fwd_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HG = Hq / 16;
+  const int64_t items = L * HG;
+  const int64_t item = items - 1 - ((int64_t)blockIdx.x * C::WARPS + warp);  // late queries first
+  if (item < 0) return;
+  const int64_t t = item / HG;
+  const int hg = (int)(item % HG);
+  const uint32_t wbase = smem_u32(fwd_smem) + warp * C::NST * C::STAGE_BYTES;
+  const int32_t* irow = idx + t * k;
+  const int nslots = k + 1;
+  const int ngroups = (nslots + 3) / 4;
+  const int g = lane >> 2, qi = lane & 3;
+
+  // Q fragments (A operand, rows = heads hg*16 .. +15).
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(Q + (t * Hq + hg * 16) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qa[ks][0] = __ldg(q32 + (g * D + ks * 16 + 2 * qi) / 2);
+      qa[ks][1] = __ldg(q32 + ((g + 8) * D + ks * 16 + 2 * qi) / 2);
+      qa[ks][2] = __ldg(q32 + (g * D + ks * 16 + 8 + 2 * qi) / 2);
+      qa[ks][3] = __ldg(q32 + ((g + 8) * D + ks * 16 + 8 + 2 * qi) / 2);
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  // prologue
+#pragma unroll
+  for (int s = 0; s < C::NST - 1; ++s) {
+    if (s < ngroups) {
+      const int64_t mp = lane < 4 ? slot_pool(irow, k, s * 4 + lane, t) : -1;
+      gather_step<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, s);
+    }
+    cp_async_commit();
+  }
+
+  for (int grp = 0; grp < ngroups; ++grp) {
+    {
+      const int nx = grp + C::NST - 1;
+      if (nx < ngroups) {
+        const int64_t mp = lane < 4 ? slot_pool(irow, k, nx * 4 + lane, t) : -1;
+        gather_step<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, nx);
+      }
+      cp_async_commit();
+    }
+    // validity of this lane's four S columns: keys nt*8 + 2*qi + {0,1}
+    const int64_t cur = lane < 4 ? slot_pool(irow, k, grp * 4 + lane, t) : -1;
+    bool kv[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int sig = nt * 2 + (qi >> 1);
+      const int64_t p = __shfl_sync(0xffffffffu, cur, sig);
+      const int slot = grp * 4 + sig;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int row = 2 * (qi & 1) + e;
+        kv[nt][e] = p >= 0 && (slot != k || 4 * p + row <= t);
+      }
+    }
+    cp_async_wait<C::NST - 1>();
+    __syncwarp();
+    const uint32_t ks_base = wbase + (grp % C::NST) * C::STAGE_BYTES;
+    const uint32_t vs_base = ks_base + C::TILE_BYTES;
+
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    {
+      const int mtx = lane >> 3, r = lane & 7;
+      const int key = (mtx >> 1) * 8 + r;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int ch = 2 * ks + (mtx & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ks_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      }
+    }
+    // online softmax (log2 domain); c0,c1 -> head g, c2,c3 -> head g+8
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = kv[nt][0] ? s[nt][0] * scale_log2 : -INFINITY;
+      s[nt][1] = kv[nt][1] ? s[nt][1] * scale_log2 : -INFINITY;
+      s[nt][2] = kv[nt][0] ? s[nt][2] * scale_log2 : -INFINITY;
+      s[nt][3] = kv[nt][1] ? s[nt][3] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
+    m0 = mn0;
+    m1 = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - base0);
+      s[nt][1] = exp2f(s[nt][1] - base0);
+      s[nt][2] = exp2f(s[nt][2] - base1);
+      s[nt][3] = exp2f(s[nt][3] - base1);
+      rs0 += s[nt][0] + s[nt][1];
+      rs1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * a0 + rs0;
+    l1 = l1 * a1 + rs1;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] *= a0;
+      o[n][1] *= a0;
+      o[n][2] *= a1;
+      o[n][3] *= a1;
+    }
+    const uint32_t pa0 = pack_bf16(s[0][0], s[0][1]), pa1 = pack_bf16(s[0][2], s[0][3]);
+    const uint32_t pa2 = pack_bf16(s[1][0], s[1][1]), pa3 = pack_bf16(s[1][2], s[1][3]);
+    {
+      const int mtx = lane >> 3, r = lane & 7;
+      const int key = (mtx & 1) * 8 + r;
+#pragma unroll
+      for (int j = 0; j < D / 16; ++j) {
+        const int ch = 2 * j + (mtx >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vs_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, b0, b1);
+        mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, b2, b3);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+  __nv_bfloat16* orow0 = O + (t * Hq + hg * 16 + g) * D;
+  __nv_bfloat16* orow1 = orow0 + 8 * D;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    *reinterpret_cast<uint32_t*>(orow0 + n * 8 + 2 * qi) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
+    *reinterpret_cast<uint32_t*>(orow1 + n * 8 + 2 * qi) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+  }
+  if (qi == 0) {
+    constexpr float kLn2 = 0.6931471805599453f;
+    LSE[t * Hq + hg * 16 + g] = (m0 + log2f(l0)) * kLn2;
+    LSE[t * Hq + hg * 16 + g + 8] = (m1 + log2f(l1)) * kLn2;
+  }
+}
+
+// ------------------------------------------------------------ fp32 (SIMT)
+// One CTA of 128 threads per query; keys in tiles of 32 staged in shared
+// memory; S, online-softmax state and O for all Hq heads kept in SMEM.
+constexpr int kF32Tile = 32;
+
+__global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const float* __restrict__ Q,
+                                                           const float* __restrict__ K,
+                                                           const float* __restrict__ V,
+                                                           const int32_t* __restrict__ idx, float* __restrict__ O,
+                                                           float* __restrict__ LSE, int64_t L, int Hq, int d,
+                                                           int k, float scale) {
+  extern __shared__ float f32_smem[];
+  float* qs = f32_smem;                    // [Hq][d]
+  float* ks = qs + Hq * d;                 // [32][d]
+  float* vs = ks + kF32Tile * d;           // [32][d]
+  float* os = vs + kF32Tile * d;           // [Hq][d]
+  float* ss = os + Hq * d;                 // [Hq][32]
+  float* ms = ss + Hq * kF32Tile;          // [Hq] running max
+  float* ls = ms + Hq;                     // [Hq] running sum
+  float* as = ls + Hq;                     // [Hq] rescale
+  int64_t* keys = reinterpret_cast<int64_t*>(as + Hq + (Hq & 1));  // [32]
+  const int64_t t = L - 1 - blockIdx.x;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < Hq * d; i += blockDim.x) {
+    qs[i] = Q[t * Hq * d + i];
+    os[i] = 0.f;
+  }
+  for (int h = tid; h < Hq; h += blockDim.x) {
+    ms[h] = -INFINITY;
+    ls[h] = 0.f;
+  }
+  const int32_t* irow = idx + t * k;
+  const int nkeys_max = 4 * (k + 1);
+  for (int kb = 0; kb < nkeys_max; kb += kF32Tile) {
+    __syncthreads();
+    if (tid < kF32Tile) {
+      const int kk = kb + tid;
+      const int slot = kk >> 2, row = kk & 3;
+      int64_t p = -1;
+      if (slot < k) {
+        p = irow[slot];
+        if (p >= elig(t)) {
+          record_error(DSA_DEV_ERR_BAD_INDEX);
+          p = -1;
+        }
+        if (p < 0) p = -1;
+      } else if (slot == k && (t & 3) != 3) {
+        p = t >> 2;
+      }
+      const int64_t tok = 4 * p + row;
+      keys[tid] = (p >= 0 && (slot != k || tok <= t)) ? tok : -1;
+    }
+    __syncthreads();
+    for (int i = tid; i < kF32Tile * d; i += blockDim.x) {
+      const int j = i / d, c = i % d;
+      const int64_t key = keys[j];
+      ks[i] = key >= 0 ? K[key * d + c] : 0.f;
+      vs[i] = key >= 0 ? V[key * d + c] : 0.f;
+    }
+    __syncthreads();
+    for (int i = tid; i < Hq * kF32Tile; i += blockDim.x) {
+      const int h = i / kF32Tile, j = i % kF32Tile;
+      float acc = 0.f;
+      for (int c = 0; c < d; ++c) acc = fmaf(qs[h * d + c], ks[j * d + c], acc);
+      ss[i] = keys[j] >= 0 ? acc * scale : -INFINITY;
+    }
+    __syncthreads();
+    for (int h = tid; h < Hq; h += blockDim.x) {
+      float mx = ms[h];
+      for (int j = 0; j < kF32Tile; ++j) mx = fmaxf(mx, ss[h * kF32Tile + j]);
+      const float base = mx == -INFINITY ? 0.f : mx;
+      const float a = expf(ms[h] - base);
+      float sum = ls[h] * a;
+      for (int j = 0; j < kF32Tile; ++j) {
+        const float pj = expf(ss[h * kF32Tile + j] - base);
+        ss[h * kF32Tile + j] = pj;
+        sum += pj;
+      }
+      ms[h] = mx;
+      ls[h] = sum;
+      as[h] = a;
+    }
+    __syncthreads();
+    for (int i = tid; i < Hq * d; i += blockDim.x) {
+      const int h = i / d, c = i % d;
+      float acc = os[i] * as[h];
+      for (int j = 0; j < kF32Tile; ++j) acc = fmaf(ss[h * kF32Tile + j], vs[j * d + c], acc);
+      os[i] = acc;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < Hq * d; i += blockDim.x) O[t * Hq * d + i] = os[i] / ls[i / d];
+  for (int h = tid; h < Hq; h += blockDim.x) LSE[t * Hq + h] = ms[h] + logf(ls[h]);
+}
+
+cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                 const void* v, const int32_t* idx, void* o, float* lse, cudaStream_t s) {
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const int64_t items = L * (Hq / 16);
+  const int64_t blocks = (items + 3) / 4;
+  auto qp = static_cast<const __nv_bfloat16*>(q);
+  auto kp = static_cast<const __nv_bfloat16*>(kk);
+  auto vp = static_cast<const __nv_bfloat16*>(v);
+  auto op = static_cast<__nv_bfloat16*>(o);
+  if (d == 128) {
+    constexpr int smem = FwdCfg<128>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_bf16_kernel<128><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
+  } else if (d == 64) {
+    constexpr int smem = FwdCfg<64>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_bf16_kernel<64><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
+  } else {
+    return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd_f32(int64_t L, int Hq, int d, int k, float scale, const float* q, const float* kk,
+                                const float* v, const int32_t* idx, float* o, float* lse, cudaStream_t s) {
+  const size_t smem = sizeof(float) * ((size_t)Hq * d * 2 + 2 * kF32Tile * d + Hq * kF32Tile + 3 * Hq + 1) +
+                      sizeof(int64_t) * kF32Tile + 16;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  attn_fwd_f32_kernel<<<(unsigned)L, 128, smem, s>>>(q, kk, v, idx, o, lse, L, Hq, d, k, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

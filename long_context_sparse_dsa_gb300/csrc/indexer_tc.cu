@@ -1,0 +1,351 @@
+// indexer_tc.cu -- lightning-indexer scores on the tcgen05 tensor cores (bf16).
+//
+// Page "SkyRL extends GLM-5.3-Flash training context to 1 million tokens",
+// section "Model and bottleneck" (every query scores one pool per 4 tokens;
+// this scoring is the layer's quadratic part) and section "1. DSA truly
+// sparse" (scored in query chunks, so the L x L/4 score matrix is never
+// materialised at once):
+//   s[t,p] = sum_h w[t,h] * max(0, q_I[t,h,:] . kpool[p,:]),   p < elig(t).
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   * MMA shape M=128 pools x N=32 queries x K=16, one MMA per indexer head:
+//     D_h[p,t] = kpool[p,:] . q_I[t,h,:], fp32 accumulators in tensor memory.
+//     The Hi heads of one 32-query block sit side by side in TMEM columns
+//     (h*32 + t), so an epilogue thread -- which owns one pool (TMEM lane) --
+//     finds all heads of a query in its own registers and applies ReLU, the
+//     head weight and the head sum without any cross-thread exchange.
+//   * Two accumulators (2 x Hi x 32 columns) let the MMAs of tile i+1 run
+//     while the epilogue drains tile i.
+//   * Warp 0 issues TMA loads (128-byte swizzle): the q_I block of a work unit
+//     (all heads, double-buffered) and a ring of kpool tiles.  Warp 1 allocates
+//     TMEM and issues the MMAs from one thread; warps 2..9 run the epilogue
+//     (two warps per TMEM lane quarter, each taking 16 of the 32 queries).
+//   * Work unit = (32-query block, up to kSeg pool tiles).  Pool tiles wholly
+//     in the future of every query of the block are never visited; the
+//     diagonal tile is masked at the store.  Units are handed out round-robin
+//     to the persistent CTAs, later (longer) query blocks first.
+//   * Every mbarrier wait is bounded; on expiry the CTA records a timeout,
+//     unwinds, and still frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace dsa {
+
+template <int HI, int DI>
+struct IdxCfg {
+  static constexpr int BM = 128;                      // pools per tile (MMA M = TMEM lanes)
+  static constexpr int BN = 32;                       // queries per block (MMA N)
+  static constexpr int KC = DI / 64;                  // 128-byte K chunks
+  static constexpr int A_CHUNK = BM * 128;            // bytes of one K chunk of a kpool tile
+  static constexpr int B_CHUNK = BN * 128;            // bytes of one (head, K chunk) of a q_I block
+  static constexpr int A_BYTES = KC * A_CHUNK;
+  static constexpr int B_BYTES = HI * KC * B_CHUNK;
+  static constexpr int NSA = DI == 64 ? 4 : 2;        // kpool tile stages
+  static constexpr int ACC_COLS = HI * BN;            // TMEM columns per accumulator
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;      // 256 or 512 (power of two)
+  static constexpr int SEG = 16;                      // pool tiles per work unit
+  static constexpr int THREADS = 320;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + NSA * A_BYTES;
+  static constexpr int OFF_W = OFF_B + 2 * B_BYTES;
+  static constexpr int OFF_BAR = OFF_W + 8 * 16 * HI * 4;  // private w slice per epilogue warp
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+};
+
+struct UnitIter {
+  int64_t q_begin, q_end, nqb, maxseg, P;
+  int64_t u, stride;
+  // current unit
+  int64_t t0, tile_begin, tile_end;
+  __device__ int64_t ntiles(int64_t qb, int BN, int BM) const {
+    int64_t t_last = q_begin + qb * BN + BN - 1;
+    if (t_last >= q_end) t_last = q_end - 1;
+    return (elig(t_last) + BM - 1) / BM;
+  }
+  template <int BN, int BM, int SEG>
+  __device__ bool next() {
+    while (u < nqb * maxseg) {
+      const int64_t seg = u / nqb;
+      const int64_t qb = nqb - 1 - (u % nqb);
+      u += stride;
+      const int64_t nt = ntiles(qb, BN, BM);
+      if (seg * SEG >= nt) continue;
+      t0 = q_begin + qb * BN;
+      tile_begin = seg * SEG;
+      tile_end = tile_begin + SEG < nt ? tile_begin + SEG : nt;
+      return true;
+    }
+    return false;
+  }
+};
+
+template <int HI, int DI>
+__global__ void __launch_bounds__(320, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
+                      const float* __restrict__ w, float* __restrict__ scores, int64_t P, int64_t q_begin,
+                      int64_t q_count) {
+  using C = IdxCfg<HI, DI>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_u32(smem + C::OFF_A);
+  const uint32_t sB = smem_u32(smem + C::OFF_B);
+  float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  // barrier slots: full_a[4] empty_a[4] full_b[2] empty_b[2] tfull[2] tempty[2]
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto empty_a = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto full_b = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * (10 + s); };
+  auto tfull = [&](int s) { return bar0 + 8u * (12 + s); };
+  auto tempty = [&](int s) { return bar0 + 8u * (14 + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  const uint32_t drain_bar = bar0 + 8u * 18;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t q_end = q_begin + q_count;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSA; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_b(s), 1);
+      mbar_init(tfull(s), 1);
+      mbar_init(tempty(s), 8);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_kp);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  UnitIter it;
+  it.q_begin = q_begin;
+  it.q_end = q_end;
+  it.nqb = (q_count + C::BN - 1) / C::BN;
+  it.P = P;
+  {
+    const int64_t nt_last = it.ntiles(it.nqb - 1, C::BN, C::BM);
+    it.maxseg = (nt_last + C::SEG - 1) / C::SEG;
+  }
+  it.u = blockIdx.x;
+  it.stride = gridDim.x;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t a_iter = 0, b_iter = 0;
+      bool ok = true;
+      while (ok && it.next<C::BN, C::BM, C::SEG>()) {
+        const int bb = b_iter & 1;
+        if (!(ok = mbar_wait(empty_b(bb), ((b_iter >> 1) & 1) ^ 1, abort_flag))) break;
+        mbar_arrive_expect_tx(full_b(bb), C::B_BYTES);
+        for (int h = 0; h < HI; ++h)
+          for (int c = 0; c < C::KC; ++c)
+            tma_load_3d(sB + bb * C::B_BYTES + (h * C::KC + c) * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, h,
+                        (int32_t)it.t0);
+        ++b_iter;
+        for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+          const int s = a_iter % C::NSA;
+          if (!(ok = mbar_wait(empty_a(s), ((a_iter / C::NSA) & 1) ^ 1, abort_flag))) break;
+          mbar_arrive_expect_tx(full_a(s), C::A_BYTES);
+          for (int c = 0; c < C::KC; ++c)
+            tma_load_2d(sA + s * C::A_BYTES + c * C::A_CHUNK, &tmap_kp, full_a(s), 64 * c,
+                        (int32_t)(tile * C::BM));
+          ++a_iter;
+        }
+      }
+      // On abort, wait (bounded) for the loads this thread issued last into
+      // each buffer, so no TMA write lands after the CTA has exited.
+      if (!ok) {
+        for (uint32_t i = (a_iter > (uint32_t)C::NSA ? a_iter - C::NSA : 0); i < a_iter; ++i)
+          mbar_wait(full_a(i % C::NSA), (i / C::NSA) & 1, nullptr);
+        for (uint32_t i = (b_iter > 2u ? b_iter - 2 : 0); i < b_iter; ++i) mbar_wait(full_b(i & 1), (i >> 1) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::BN);
+      uint32_t a_iter = 0, b_iter = 0, acc_iter = 0;
+      bool ok = true;
+      while (ok && it.next<C::BN, C::BM, C::SEG>()) {
+        const int bb = b_iter & 1;
+        if (!(ok = mbar_wait(full_b(bb), (b_iter >> 1) & 1, abort_flag))) break;
+        for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+          const int s = a_iter % C::NSA;
+          const int ab = acc_iter & 1;
+          if (!(ok = mbar_wait(full_a(s), (a_iter / C::NSA) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(tempty(ab), ((acc_iter >> 1) & 1) ^ 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t d_base = tmem_base + ab * C::ACC_COLS;
+#pragma unroll
+          for (int c = 0; c < C::KC; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(sA + s * C::A_BYTES + c * C::A_CHUNK + kk * 32);
+#pragma unroll
+              for (int h = 0; h < HI; ++h) {
+                const uint64_t bdesc =
+                    smem_desc_sw128(sB + bb * C::B_BYTES + (h * C::KC + c) * C::B_CHUNK + kk * 32);
+                tc_mma_f16(d_base + h * C::BN, adesc, bdesc, idesc, (c | kk) != 0);
+              }
+            }
+          }
+          tc_commit(empty_a(s));
+          tc_commit(tfull(ab));
+          ++a_iter;
+          ++acc_iter;
+        }
+        if (!ok) break;
+        tc_commit(empty_b(bb));
+        ++b_iter;
+      }
+      // Drain: wait (bounded) until every MMA this thread issued has finished,
+      // so tensor memory is never freed under a running MMA.
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0, nullptr);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int ew = warp - 2;                 // 0..7
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int half = ew >> 2;                // which 16 of the 32 queries
+    const int lane_base = quarter * 32;
+    uint32_t acc_iter = 0;
+    bool ok = true;
+    float* w_mine = w_s + ew * 16 * HI;      // this warp's 16 queries x HI weights
+    while (ok && it.next<C::BN, C::BM, C::SEG>()) {
+      __syncwarp();
+      for (int i = lane; i < 16 * HI; i += 32) {
+        const int64_t t = it.t0 + half * 16 + i / HI;
+        w_mine[i] = t < q_end ? __ldg(w + t * HI + (i % HI)) : 0.f;
+      }
+      __syncwarp();
+      for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+        const int ab = acc_iter & 1;
+        if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16;
+#pragma unroll
+        for (int h = 0; h < HI; h += 2) {
+          float v0[16], v1[16];
+          tmem_ld16(taddr + h * C::BN, v0);
+          tmem_ld16(taddr + (h + 1) * C::BN, v1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(fmaxf(v0[j], 0.f), w_mine[j * HI + h], acc[j]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] = fmaf(fmaxf(v1[j], 0.f), w_mine[j * HI + h + 1], acc[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(ab));
+        const int64_t p = tile * C::BM + lane_base + lane;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int64_t t = it.t0 + half * 16 + j;
+          if (t < q_end && p < elig(t)) scores[(t - q_begin) * P + p] = acc[j];
+        }
+        ++acc_iter;
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int HI, int DI>
+static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, const float* w, int64_t q_begin,
+                             int64_t q_count, float* scores, cudaStream_t s) {
+  using C = IdxCfg<HI, DI>;
+  const int64_t P = L / 4;
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tq, tk;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)HI, (cuuint64_t)L};
+    const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)HI * DI * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)C::BN};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)P};
+    const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)C::BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kpool), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t nqb = (q_count + C::BN - 1) / C::BN;
+  int64_t t_last = q_begin + q_count - 1;
+  const int64_t nt_last = (((t_last + 1) >> 2) + C::BM - 1) / C::BM;
+  const int64_t units = nqb * ((nt_last + C::SEG - 1) / C::SEG);
+  if (units == 0) return cudaSuccess;
+  int64_t grid = device_sm_count();
+  if (grid > units) grid = units;
+  indexer_tc_kernel<HI, DI><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, w, scores, P, q_begin,
+                                                                               q_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_tc_bf16(int64_t L, int Hi, int di, const void* q_idx, const void* kpool,
+                                   const float* w, int64_t q_begin, int64_t q_count, float* scores,
+                                   cudaStream_t s) {
+  if (Hi == 8 && di == 64) return launch_tc<8, 64>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
+  if (Hi == 8 && di == 128) return launch_tc<8, 128>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
+  if (Hi == 4 && di == 64) return launch_tc<4, 64>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
+  if (Hi == 4 && di == 128) return launch_tc<4, 128>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace dsa

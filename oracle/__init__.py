@@ -56,9 +56,9 @@ def _load():
             lib.oracle_topk.restype = ctypes.c_int
             lib.oracle_key_set.argtypes = [i64, P, i32, P]
             lib.oracle_key_set.restype = i64
-            lib.oracle_attn_fwd.argtypes = [i64, i32, i32, f64, P, P, P, P, i32, P, i64, P, P]
+            lib.oracle_attn_fwd.argtypes = [i64, i32, i32, f64, P, i32, P, P, P, i32, P, i64, P, P]
             lib.oracle_attn_fwd.restype = ctypes.c_int
-            lib.oracle_attn_bwd.argtypes = [i64, i32, i32, f64, P, P, P, P, i32, P, P, i64, P, P, P]
+            lib.oracle_attn_bwd.argtypes = [i64, i32, i32, f64, P, i32, P, P, P, i32, P, P, i64, P, P, P]
             lib.oracle_attn_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -129,23 +129,31 @@ def key_set(t: int, idx_row, k: int) -> np.ndarray:
     return keys[:n].copy()
 
 
-def attn_fwd(Q, K, V, idx, scale: float, rows=None):
-    """O [len(rows), Hq, d] and LSE [len(rows), Hq], fp64.  idx: full [L, k]."""
+def attn_fwd(Q, K, V, idx, scale: float, rows=None, q_compact: bool = False):
+    """O [len(rows), Hq, d] and LSE [len(rows), Hq], fp64.  idx: full [L, k].
+
+    With q_compact, Q holds only the listed rows ([len(rows), Hq, d])."""
     Q, K, V = _f32(Q), _f32(K), _f32(V)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
-    L, Hq, d = Q.shape
+    L = K.shape[0]
+    Hq, d = Q.shape[1], Q.shape[2]
     k = idx.shape[1]
     r = _rows(rows, L)
+    if q_compact:
+        assert Q.shape[0] == r.size
+    else:
+        assert Q.shape[0] == L
     O = np.empty((r.size, Hq, d), np.float64)
     LSE = np.empty((r.size, Hq), np.float64)
-    rc = _load().oracle_attn_fwd(L, Hq, d, float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(idx), k,
+    rc = _load().oracle_attn_fwd(L, Hq, d, float(scale), _ptr(Q), int(q_compact), _ptr(K), _ptr(V), _ptr(idx), k,
                                  _ptr(r), r.size, _ptr(O), _ptr(LSE))
     if rc:
         raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
     return O, LSE
 
 
-def attn_bwd(Q, K, V, idx, dO, scale: float, rows=None, with_dkv: bool = True, threads: int = 1):
+def attn_bwd(Q, K, V, idx, dO, scale: float, rows=None, with_dkv: bool = True, threads: int = 1,
+             q_compact: bool = False):
     """dQ [len(rows), Hq, d]; dK, dV [L, d] summed over the listed rows (fp64).
 
     With threads > 1 the rows are split into `threads` contiguous shards, each
@@ -154,9 +162,12 @@ def attn_bwd(Q, K, V, idx, dO, scale: float, rows=None, with_dkv: bool = True, t
     """
     Q, K, V, dO = _f32(Q), _f32(K), _f32(V), _f32(dO)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
-    L, Hq, d = Q.shape
+    L = K.shape[0]
+    Hq, d = Q.shape[1], Q.shape[2]
     k = idx.shape[1]
     r = _rows(rows, L)
+    if q_compact:
+        assert Q.shape[0] == r.size and dO.shape[0] == r.size
     lib = _load()
     dQ = np.zeros((r.size, Hq, d), np.float64)
     nshard = max(1, min(int(threads), r.size if r.size else 1))
@@ -168,7 +179,10 @@ def attn_bwd(Q, K, V, idx, dO, scale: float, rows=None, with_dkv: bool = True, t
         a, b = int(bounds[s]), int(bounds[s + 1])
         rr = np.ascontiguousarray(r[a:b])
         dq = np.zeros((b - a, Hq, d), np.float64)
-        rc = lib.oracle_attn_bwd(L, Hq, d, float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(idx), k, _ptr(dO),
+        Qs = np.ascontiguousarray(Q[a:b]) if q_compact else Q
+        dOs = np.ascontiguousarray(dO[a:b]) if q_compact else dO
+        rc = lib.oracle_attn_bwd(L, Hq, d, float(scale), _ptr(Qs), int(q_compact), _ptr(K), _ptr(V), _ptr(idx), k,
+                                 _ptr(dOs),
                                  _ptr(rr), rr.size, _ptr(dq),
                                  _ptr(dKs[s]) if with_dkv else None, _ptr(dVs[s]) if with_dkv else None)
         if rc:
@@ -204,3 +218,31 @@ def layer_fwd(Q, K, V, q_I, k_I, w, k: int, scale: float, round_to_bf16: bool, r
     idx_full[r] = idx_rows
     O, LSE = attn_fwd(Q, K, V, idx_full, scale, r)
     return kpool, idx_rows, O, LSE
+
+
+def select_rows(q_I, kpool, w, k: int, rows, threads: int = 1, block: int = 128) -> np.ndarray:
+    """Top-k selection for the listed rows, scored and selected block by block
+    (bounded memory), optionally over several threads.  Pure orchestration of
+    indexer_scores and topk."""
+    q_I, kpool, w = _f32(q_I), _f32(kpool), _f32(w)
+    L = q_I.shape[0]
+    r = _rows(rows, L)
+    out = np.empty((r.size, k), np.int32)
+    starts = list(range(0, r.size, block))
+
+    def run(a):
+        rr = r[a:a + block]
+        out[a:a + rr.size] = topk(indexer_scores(q_I, kpool, w, rr), L, k, rr)
+
+    if threads <= 1:
+        for a in starts:
+            run(a)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, starts))
+    return out
+
+
+def scores_for(q_I, kpool, w, rows) -> np.ndarray:
+    """fp64 indexer scores for the listed rows (alias kept for readability at call sites)."""
+    return indexer_scores(q_I, kpool, w, rows)

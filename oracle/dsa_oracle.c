@@ -180,10 +180,11 @@ int64_t oracle_key_set(int64_t t, const int32_t *idx_row, int32_t k, int64_t *ke
     return n;
 }
 
-/* Sparse attention forward for the listed rows.  Q: [L, Hq, d]; K, V: [L, d];
- * idx: [L, k]; O: [nrows, Hq, d]; LSE: [nrows, Hq]. */
+/* Sparse attention forward for the listed rows.  Q: [L, Hq, d], or
+ * [nrows, Hq, d] holding only the listed rows when q_compact != 0;
+ * K, V: [L, d]; idx: [L, k]; O: [nrows, Hq, d]; LSE: [nrows, Hq]. */
 int oracle_attn_fwd(int64_t L, int32_t Hq, int32_t d, double scale,
-                    const float *Q, const float *K, const float *V,
+                    const float *Q, int32_t q_compact, const float *K, const float *V,
                     const int32_t *idx, int32_t k,
                     const int64_t *rows, int64_t nrows, double *O, double *LSE)
 {
@@ -197,7 +198,7 @@ int oracle_attn_fwd(int64_t L, int32_t Hq, int32_t d, double scale,
         int64_t n = oracle_key_set(t, idx + t * k, k, keys);
         if (n < 0) { rc = ORACLE_BAD_INDEX; break; }
         for (int32_t h = 0; h < Hq; ++h) {
-            const float *q = Q + (t * Hq + h) * d;
+            const float *q = Q + ((q_compact ? r : t) * Hq + h) * d;
             double m = -INFINITY;
             for (int64_t j = 0; j < n; ++j) {
                 double dot = 0.0;
@@ -222,12 +223,13 @@ int oracle_attn_fwd(int64_t L, int32_t Hq, int32_t d, double scale,
 }
 
 /* Sparse attention backward for the listed rows, given the upstream gradient
- * dO: [L, Hq, d].  Writes dQ: [nrows, Hq, d]; when dK and dV ([L, d]) are not
+ * dO: [L, Hq, d] (Q and dO hold only the listed rows, [nrows, Hq, d], when
+ * q_compact != 0).  Writes dQ: [nrows, Hq, d]; when dK and dV ([L, d]) are not
  * NULL, ADDS this rows' contributions to them (the caller zeroes them, and
  * may sum several disjoint row sets).  Uses its own double-precision O and
  * LSE.  No gradient flows to the indexer inputs. */
 int oracle_attn_bwd(int64_t L, int32_t Hq, int32_t d, double scale,
-                    const float *Q, const float *K, const float *V,
+                    const float *Q, int32_t q_compact, const float *K, const float *V,
                     const int32_t *idx, int32_t k, const float *dO,
                     const int64_t *rows, int64_t nrows,
                     double *dQ, double *dK, double *dV)
@@ -243,8 +245,9 @@ int oracle_attn_bwd(int64_t L, int32_t Hq, int32_t d, double scale,
         int64_t n = oracle_key_set(t, idx + t * k, k, keys);
         if (n < 0) { rc = ORACLE_BAD_INDEX; break; }
         for (int32_t h = 0; h < Hq; ++h) {
-            const float *q = Q + (t * Hq + h) * d;
-            const float *go = dO + (t * Hq + h) * d;
+            const int64_t qr = q_compact ? r : t;
+            const float *q = Q + (qr * Hq + h) * d;
+            const float *go = dO + (qr * Hq + h) * d;
             double m = -INFINITY;
             for (int64_t j = 0; j < n; ++j) {
                 double dot = 0.0;

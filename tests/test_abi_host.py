@@ -1,0 +1,91 @@
+"""Host-only checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/dsa.h declares, and rejects bad arguments before any
+launch (so none of these calls touches a GPU)."""
+import ctypes
+
+import pytest
+
+from long_context_sparse_dsa_gb300 import build as dsa_build
+
+dsa = pytest.importorskip("long_context_sparse_dsa_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return dsa.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = dsa.header_functions()
+    assert {"dsa_pool_keys", "dsa_indexer_score", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd",
+            "dsa_layer_fwd", "dsa_layer_bwd", "dsa_check_device_error", "dsa_workspace_bytes"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert dsa.status_string(s) not in ("", "unknown status")
+    assert dsa.status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(L=4096, Hq=16, d=128, Hi=8, di=64, k=512, q_chunk=1024, dtype="bf16")
+    base.update(kw)
+    return dsa.make_dims(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), dsa.DSA_OK),
+    (dict(L=4094), dsa.DSA_ERR_INVALID_ARG),
+    (dict(L=0), dsa.DSA_ERR_INVALID_ARG),
+    (dict(k=0), dsa.DSA_ERR_INVALID_ARG),
+    (dict(q_chunk=0), dsa.DSA_ERR_INVALID_ARG),
+    (dict(d=96), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(di=32), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(Hq=8), dsa.DSA_ERR_UNSUPPORTED),          # bf16 needs 16 or 32 heads: no silent fallback
+    (dict(Hi=6), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(k=2048), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(pool=8), dsa.DSA_ERR_UNSUPPORTED),
+    (dict(Hq=8, dtype="fp32"), dsa.DSA_OK),
+    (dict(Hq=3, Hi=3, dtype="fp32"), dsa.DSA_OK),
+])
+def test_validate_dims(lib, kw, status):
+    assert dsa.validate_dims(_dims(**kw)) == status
+
+
+def test_fp32_backward_is_rejected_not_faked(lib):
+    assert dsa.validate_dims(_dims(Hq=8, dtype="fp32"), with_backward=True) == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_workspace_bytes(lib):
+    assert dsa.workspace_bytes(_dims(L=131072, q_chunk=8192)) == 8192 * 32768 * 4
+    assert dsa.workspace_bytes(_dims(L=4096, q_chunk=100)) == (100 * 1024 * 4 + 255) // 256 * 256
+    assert dsa.workspace_bytes(_dims(L=4094)) == 0
+
+
+def test_null_and_misaligned_pointers_fail_before_launch(lib):
+    d = _dims()
+    assert lib.dsa_pool_keys(ctypes.byref(d), None, ctypes.c_void_p(256), None) == dsa.DSA_ERR_INVALID_ARG
+    assert b"k_idx" in lib.dsa_last_error_message()
+    assert lib.dsa_pool_keys(ctypes.byref(d), ctypes.c_void_p(264), ctypes.c_void_p(256), None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert b"aligned" in lib.dsa_last_error_message()
+    assert lib.dsa_indexer_score(ctypes.byref(d), 256, 256, 256, 4000, 200, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_topk(ctypes.byref(d), 256, -1, 10, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    # too small a workspace is reported as such
+    p = ctypes.c_void_p(256)
+    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, p, 16, None) == dsa.DSA_ERR_WORKSPACE
+    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, None, 1 << 40, None) == \
+        dsa.DSA_ERR_WORKSPACE
+    # aliased gradient outputs
+    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, None, 0, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_bounded_wait(0, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_binding_has_no_cpu_path():
+    import inspect
+    src = inspect.getsource(dsa)
+    assert "oracle" not in src and "numpy" not in src

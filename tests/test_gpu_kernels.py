@@ -1,0 +1,229 @@
+"""GPU parity of each kernel against the CPU oracle (through the C ABI).
+
+Sizes span several tiles and a ragged tail: pool counts that are not a
+multiple of the 128-pool MMA tile, query ranges that start and end off the
+32-query block, score rows on both sides of the top-k shared-memory staging
+limit, keys sets below k.  Integer-valued indexer inputs make every fp32 score
+exact, so pool keys, scores and top-k are compared bit for bit; attention is
+compared by max-abs error against the fp64 oracle (2e-2 bf16, 1e-4 fp32).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import long_context_sparse_dsa_gb300 as dsa
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = {"bf16": 2e-2, "fp32": 1e-4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_sparse_dsa_gb300 import build
+    build.build()
+    dsa.library()
+
+
+def _tdt(dtype):
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def _f32(t):
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def _int_inputs(g, L, Hi, di, dtype):
+    q = torch.randint(-3, 4, (L, Hi, di), generator=g).to(_tdt(dtype))
+    k = torch.randint(-3, 4, (L, di), generator=g).to(_tdt(dtype))
+    w = torch.randint(1, 5, (L, Hi), generator=g).to(torch.float32)
+    return q, k, w
+
+
+def _sentinel(shape):
+    return torch.full(shape, 0x7fc0dead, dtype=torch.int32, device=DEV).view(torch.float32)
+
+
+# ---------------------------------------------------------------- selftest
+def test_bounded_wait_gives_up_and_stream_survives():
+    dsa.check_device_error()
+    dsa.selftest_bounded_wait(2000)
+    with pytest.raises(dsa.DSAError) as e:
+        dsa.check_device_error()
+    assert e.value.status == dsa.DSA_ERR_TIMEOUT
+    x = torch.arange(16, device=DEV, dtype=torch.float32)
+    assert float((x * 2).sum()) == 240.0
+    dsa.check_device_error()
+
+
+# ---------------------------------------------------------------- pool keys
+@pytest.mark.parametrize("dtype,di", [("bf16", 64), ("bf16", 128), ("fp32", 64), ("fp32", 128)])
+def test_pool_keys_bitexact(dtype, di):
+    g = torch.Generator().manual_seed(1)
+    L = 4 * 1331
+    k_I = (torch.randn(L, di, generator=g) * 3).to(_tdt(dtype))
+    dims = dsa.make_dims(L, 16 if dtype == "bf16" else 8, 128, 8, di, 8, dtype=dtype)
+    kp = torch.empty((L // 4, di), dtype=_tdt(dtype), device=DEV)
+    dsa.pool_keys(dims, k_I.to(DEV), kp)
+    ref = oracle.pool_keys(_f32(k_I), dtype == "bf16")
+    assert np.array_equal(_f32(kp).view(np.uint32), ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------- indexer
+@pytest.mark.parametrize("dtype,Hi,di", [("bf16", 8, 64), ("bf16", 8, 128), ("bf16", 4, 64), ("bf16", 4, 128),
+                                         ("fp32", 4, 64), ("fp32", 3, 128)])
+@pytest.mark.parametrize("q_begin,q_count", [(0, None), (37, 701)])
+def test_indexer_integer_inputs_bitexact(dtype, Hi, di, q_begin, q_count):
+    g = torch.Generator().manual_seed(2)
+    L = 4 * 330 + 4 * 200   # P = 530: four full 128-pool tiles and a ragged one
+    q_count = L - q_begin if q_count is None else q_count
+    q_I, k_I, w = _int_inputs(g, L, Hi, di, dtype)
+    dims = dsa.make_dims(L, 16 if dtype == "bf16" else 8, 128, Hi, di, 16, dtype=dtype)
+    P = L // 4
+    kp = torch.empty((P, di), dtype=_tdt(dtype), device=DEV)
+    dsa.pool_keys(dims, k_I.to(DEV), kp)
+    sc = _sentinel((q_count, P))
+    dsa.indexer_score(dims, q_I.to(DEV), kp, w.to(DEV), q_begin, q_count, sc)
+    dsa.check_device_error()
+    rows = np.arange(q_begin, q_begin + q_count)
+    ref = oracle.indexer_scores(_f32(q_I), oracle.pool_keys(_f32(k_I), dtype == "bf16"), _f32(w), rows)
+    got = sc.cpu().numpy()
+    e = (rows + 1) // 4
+    mask = np.arange(P)[None, :] < e[:, None]
+    assert np.array_equal(got[mask].astype(np.float64), ref[mask])
+    assert np.all(got.view(np.uint32)[~mask] == 0x7fc0dead)   # nothing written outside the causal prefix
+
+
+def test_indexer_normal_inputs_within_fp32_bound():
+    g = torch.Generator().manual_seed(3)
+    L, Hi, di = 4096, 8, 64
+    q_I = torch.randn(L, Hi, di, generator=g).to(torch.bfloat16)
+    k_I = torch.randn(L, di, generator=g).to(torch.bfloat16)
+    w = torch.rand(L, Hi, generator=g)
+    dims = dsa.make_dims(L, 16, 128, Hi, di, 512)
+    kp = torch.empty((L // 4, di), dtype=torch.bfloat16, device=DEV)
+    dsa.pool_keys(dims, k_I.to(DEV), kp)
+    sc = torch.zeros((L, L // 4), device=DEV)
+    dsa.indexer_score(dims, q_I.to(DEV), kp, w.to(DEV), 0, L, sc)
+    rows = np.arange(0, L, 7)
+    kpn = oracle.pool_keys(_f32(k_I), True)
+    ref = oracle.indexer_scores(_f32(q_I), kpn, _f32(w), rows)
+    # |error| <= (di + Hi + 2) u sum_h |w| sum_i |q_i kp_i|, u = 2^-24 (products of bf16 are exact in fp32)
+    absdot = np.einsum("thi,pi->thp", np.abs(_f32(q_I)[rows]).astype(np.float64), np.abs(kpn).astype(np.float64))
+    bound = (di + Hi + 2) * 2.0 ** -24 * np.einsum("th,thp->tp", np.abs(_f32(w)[rows]), absdot)
+    got = sc.cpu().numpy()[rows].astype(np.float64)
+    e = (rows + 1) // 4
+    mask = np.arange(L // 4)[None, :] < e[:, None]
+    err = np.abs(got - ref)
+    assert np.all(err[mask] <= 4 * bound[mask] + 1e-30), float((err[mask] / (bound[mask] + 1e-30)).max())
+
+
+# ---------------------------------------------------------------- top-k
+def _topk_case(P, rows, k, kind, seed):
+    g = torch.Generator().manual_seed(seed)
+    n = len(rows)
+    if kind == "ties":
+        s = torch.randint(-3, 4, (n, P), generator=g).to(torch.float32)
+    elif kind == "signed_zero":
+        s = torch.randint(-1, 2, (n, P), generator=g).to(torch.float32) * 0.0   # +0 and -0 only
+        s[:, ::17] = -1.5
+    else:
+        s = torch.randn(n, P, generator=g) * 10
+    return s
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "signed_zero"])
+@pytest.mark.parametrize("k", [64, 512])
+def test_topk_bitexact(kind, k):
+    L = 4 * 14000          # rows up to 14000 pools: both sides of the 12288-score staging limit
+    P = L // 4
+    dims = dsa.make_dims(L, 16, 128, 8, 64, k)
+    for (q_begin, q_count) in ((0, 300), (2000, 97), (L - 40, 40), (4 * 12288 - 20, 40)):
+        rows = np.arange(q_begin, q_begin + q_count)
+        s = _topk_case(P, rows, k, kind, seed=q_begin + k)
+        idx = torch.full((L, k), -7, dtype=torch.int32, device=DEV)
+        dsa.topk(dims, s.to(DEV), q_begin, q_count, idx)
+        got = idx.cpu().numpy()[rows]
+        sn = s.numpy().astype(np.float64)
+        e = (rows + 1) // 4
+        sn[np.arange(P)[None, :] >= e[:, None]] = np.nan
+        ref = oracle.topk(sn, L, k, rows)
+        assert np.array_equal(got, ref), (q_begin, np.argwhere(got != ref)[:5])
+        untouched = np.setdiff1d(np.arange(L), rows)[:50]
+        assert np.all(idx.cpu().numpy()[untouched] == -7)
+
+
+# ---------------------------------------------------------------- attention
+def _attn_case(L, Hq, d, k, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    dt = _tdt(dtype)
+    Q = torch.randn(L, Hq, d, generator=g).to(dt)
+    K = torch.randn(L, d, generator=g).to(dt)
+    V = torch.randn(L, d, generator=g).to(dt)
+    dO = torch.randn(L, Hq, d, generator=g).to(dt)
+    q_I, k_I, w = _int_inputs(g, L, 2, 16, "fp32")
+    idx = oracle.topk(oracle.indexer_scores(_f32(q_I), oracle.pool_keys(_f32(k_I), False), _f32(w)), L, k)
+    return Q, K, V, dO, idx
+
+
+@pytest.mark.parametrize("dtype,Hq,d", [("bf16", 16, 128), ("bf16", 32, 128), ("bf16", 16, 64), ("fp32", 8, 64),
+                                        ("fp32", 5, 128)])
+@pytest.mark.parametrize("k", [1, 5, 32])
+def test_attn_fwd_matches_oracle(dtype, Hq, d, k):
+    L = 1000
+    Q, K, V, _, idx = _attn_case(L, Hq, d, k, dtype, seed=10 + k)
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale, dtype=dtype)
+    O = torch.empty((L, Hq, d), dtype=_tdt(dtype), device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    dsa.sparse_attn_fwd(dims, Q.to(DEV), K.to(DEV), V.to(DEV), torch.from_numpy(idx).to(DEV), O, lse)
+    dsa.check_device_error()
+    Or, LSEr = oracle.attn_fwd(_f32(Q), _f32(K), _f32(V), idx, scale)
+    assert np.abs(_f32(O) - Or).max() <= TOL[dtype]
+    assert np.abs(lse.cpu().numpy() - LSEr).max() <= (1e-3 if dtype == "bf16" else 1e-4)
+
+
+@pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64)])
+@pytest.mark.parametrize("k", [3, 32])
+def test_attn_bwd_matches_oracle(Hq, d, k):
+    L = 1000
+    Q, K, V, dO, idx = _attn_case(L, Hq, d, k, "bf16", seed=20 + k)
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale)
+    dev = [t.to(DEV) for t in (Q, K, V, dO)]
+    idx_d = torch.from_numpy(idx).to(DEV)
+    O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse)
+    dq = torch.empty((L, Hq, d), device=DEV)
+    dk = torch.full((L, d), 5.0, device=DEV)     # must be overwritten, not accumulated into
+    dv = torch.full((L, d), 5.0, device=DEV)
+    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv)
+    dsa.check_device_error()
+    dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
+    errs = {name: float(np.abs(got.cpu().numpy() - ref).max())
+            for name, got, ref in (("dQ", dq, dQr), ("dK", dk, dKr), ("dV", dv, dVr))}
+    assert max(errs.values()) <= 2e-2, errs
+
+
+def test_attn_bad_index_is_skipped_and_reported():
+    L, Hq, d, k = 256, 16, 128, 4
+    Q, K, V, _, idx = _attn_case(L, Hq, d, k, "bf16", seed=5)
+    idx = idx.copy()
+    idx[200, 0] = 10_000          # beyond the sequence
+    idx[100, 1] = 30              # pool 30 ends at token 123 > 100: the future
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k)
+    O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    dsa.sparse_attn_fwd(dims, Q.to(DEV), K.to(DEV), V.to(DEV), torch.from_numpy(idx).to(DEV), O, lse)
+    with pytest.raises(dsa.DSAError) as e:
+        dsa.check_device_error()
+    assert e.value.status == dsa.DSA_ERR_BAD_INDEX
+    clean = idx.copy()
+    clean[200, 0] = -1
+    clean[100, 1] = -1
+    Or, _ = oracle.attn_fwd(_f32(Q), _f32(K), _f32(V), clean, 1 / math.sqrt(d), rows=[100, 200])
+    assert np.abs(_f32(O)[[100, 200]] - Or).max() <= 2e-2
