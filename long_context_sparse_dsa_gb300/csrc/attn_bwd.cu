@@ -127,27 +127,6 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       *reinterpret_cast<uint4*>(dsp + off) = bf16x8_to_f16x8(__ldg(d4 + c));
     }
   }
-  // D[h] = dO[h] . O[h] for the 16 heads: lane pair (2h, 2h+1) splits row h.
-  float Dg, Dg8;
-  {
-    const int h = lane >> 1, half = lane & 1;
-    const uint4* o4 = reinterpret_cast<const uint4*>(O + (row0 + h) * D) + half * (C::CHUNKS / 2);
-    const uint4* d4 = reinterpret_cast<const uint4*>(dO + (row0 + h) * D) + half * (C::CHUNKS / 2);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < C::CHUNKS / 2; ++c) {
-      const uint4 a = __ldg(o4 + c), b = __ldg(d4 + c);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
-        acc = fmaf(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
-      }
-    }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    Dg = __shfl_sync(0xffffffffu, acc, 2 * g);
-    Dg8 = __shfl_sync(0xffffffffu, acc, 2 * (g + 8));
-  }
   constexpr float kLog2e = 1.4426950408889634f;
   const float lse_g = __ldg(LSE + row0 + g) * kLog2e;
   const float lse_g8 = __ldg(LSE + row0 + g + 8) * kLog2e;
@@ -176,21 +155,30 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) dq[n][0] = dq[n][1] = dq[n][2] = dq[n][3] = 0.f;
 
+  // Two passes over the key groups through one gather pipeline: pass 1 forms
+  // D[h] = sum_j P_j dP_j (equal to dO . O, but from the exact P and dP rather
+  // than the bf16-rounded O), pass 2 forms dS and the gradients.
+  const int nsteps = 2 * ngroups;
 #pragma unroll
   for (int s = 0; s < C::NST - 1; ++s) {
-    if (s < ngroups) {
-      const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, s * 4 + lane, t) : -1;
-      bwd_gather<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, s);
+    if (s < nsteps) {
+      const int grp_s = s % ngroups;
+      const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, grp_s * 4 + lane, t) : -1;
+      bwd_gather<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, grp_s);
     }
     cp_async_commit();
   }
+  float Dg = 0.f, Dg8 = 0.f;
 
-  for (int grp = 0; grp < ngroups; ++grp) {
+  for (int step = 0; step < nsteps; ++step) {
+    const bool pass1 = step < ngroups;
+    const int grp = pass1 ? step : step - ngroups;
     {
-      const int nx = grp + C::NST - 1;
-      if (nx < ngroups) {
-        const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, nx * 4 + lane, t) : -1;
-        bwd_gather<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, nx);
+      const int nx = step + C::NST - 1;
+      if (nx < nsteps) {
+        const int grp_n = nx % ngroups;
+        const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, grp_n * 4 + lane, t) : -1;
+        bwd_gather<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, grp_n);
       }
       cp_async_commit();
     }
@@ -216,7 +204,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
-    const uint32_t ks_base = wbase + (grp % C::NST) * C::STAGE_BYTES;
+    const uint32_t ks_base = wbase + (step % C::NST) * C::STAGE_BYTES;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
     // S = Q K^T and dP = dO V^T (heads x 16 keys)
@@ -240,6 +228,28 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         mma_bf16_16816(dp[0], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b0, b1);
         mma_bf16_16816(dp[1], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b2, b3);
       }
+    }
+    if (pass1) {
+      // D partial sums over this lane's columns: rows g and g+8
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (kv[nt][0]) {
+          Dg = fmaf(exp2f(s[nt][0] * scale_log2 - lse_g), dp[nt][0], Dg);
+          Dg8 = fmaf(exp2f(s[nt][2] * scale_log2 - lse_g8), dp[nt][2], Dg8);
+        }
+        if (kv[nt][1]) {
+          Dg = fmaf(exp2f(s[nt][1] * scale_log2 - lse_g), dp[nt][1], Dg);
+          Dg8 = fmaf(exp2f(s[nt][3] * scale_log2 - lse_g8), dp[nt][3], Dg8);
+        }
+      }
+      if (step == ngroups - 1) {
+        Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
+        Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);
+        Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 1);
+        Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 2);
+      }
+      __syncwarp();
+      continue;
     }
     // P and scale*dS: bf16 for the dQ product, fp16 for dK/dV (rows g: elements 0,1; rows g+8: 2,3)
     uint32_t pp[2][2], dd[2][2], dh[2][2];
