@@ -22,37 +22,22 @@
 // global memory with fp32 vector reductions (red.global.add.v2.f32), so the
 // summation order across queries is not fixed.
 #include "common.cuh"
+#include "gather.cuh"
 #include "launch.h"
 
 namespace dsa {
 
 template <int D>
 struct BwdCfg {
-  static constexpr int KEYS = 16;
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int CHUNKS = D / 8;
-  static constexpr int TILE_BYTES = KEYS * ROW_BYTES;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int ROW_BYTES = GatherCfg<D>::ROW_BYTES;
+  static constexpr int CHUNKS = GatherCfg<D>::CHUNKS;
+  static constexpr int TILE_BYTES = GatherCfg<D>::TILE_BYTES;
+  static constexpr int STAGE_BYTES = GatherCfg<D>::STAGE_BYTES;
   static constexpr int NST = 2;
   static constexpr int WARPS = 4;
   static constexpr int WARP_BYTES = NST * STAGE_BYTES + 2 * TILE_BYTES;  // stages + Q + dO copies
   static constexpr int SMEM = WARPS * WARP_BYTES;
-  static constexpr int COPIES = 2 * KEYS * CHUNKS / 32;
 };
-
-__device__ __forceinline__ int64_t bwd_slot_pool(const int32_t* irow, int k, int slot, int64_t t) {
-  if (slot < k) {
-    const int64_t p = __ldg(irow + slot);
-    if (p < 0) return -1;
-    if (p >= elig(t)) {
-      record_error(DSA_DEV_ERR_BAD_INDEX);
-      return -1;
-    }
-    return p;
-  }
-  if (slot == k && (t & 3) != 3) return t >> 2;
-  return -1;
-}
 
 // Eight bf16 values -> eight fp16 values (exact for |x| in [2^-14, 65504]).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
@@ -62,31 +47,6 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   for (int i = 0; i < 4; ++i)
     out[i] = pack_f16(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
   return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
-template <int D>
-__device__ __forceinline__ void bwd_gather(uint32_t stage, const __nv_bfloat16* __restrict__ K,
-                                           const __nv_bfloat16* __restrict__ V, int64_t my_pool, int lane,
-                                           int64_t t, int k, int group) {
-  using C = BwdCfg<D>;
-#pragma unroll
-  for (int i = 0; i < C::COPIES; ++i) {
-    const int cid = i * 32 + lane;
-    const int sig = cid / (8 * C::CHUNKS);
-    const int rem = cid % (8 * C::CHUNKS);
-    const int tensor = rem / (4 * C::CHUNKS);
-    const int rr = rem % (4 * C::CHUNKS);
-    const int row = rr / C::CHUNKS;
-    const int ch = rr % C::CHUNKS;
-    const int64_t p = __shfl_sync(0xffffffffu, my_pool, sig);
-    const int slot = group * 4 + sig;
-    const int64_t tok = 4 * p + row;
-    const bool valid = p >= 0 && (slot != k || tok <= t);
-    const __nv_bfloat16* src = (tensor ? V : K) + (valid ? tok * D + ch * 8 : 0);
-    const int key = sig * 4 + row;
-    cp_async16(stage + tensor * C::TILE_BYTES + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), src,
-               valid ? 16u : 0u);
-  }
 }
 
 template <int D>
@@ -158,53 +118,51 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   // Two passes over the key groups through one gather pipeline: pass 1 forms
   // D[h] = sum_j P_j dP_j (equal to dO . O, but from the exact P and dP rather
   // than the bf16-rounded O), pass 2 forms dS and the gradients.
+  static_assert(C::NST == 2, "the pool ring below is written for two stages");
+  const GatherLane<D> gl = gather_lane<D>(lane);
   const int nsteps = 2 * ngroups;
-#pragma unroll
-  for (int s = 0; s < C::NST - 1; ++s) {
-    if (s < nsteps) {
-      const int grp_s = s % ngroups;
-      const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, grp_s * 4 + lane, t) : -1;
-      bwd_gather<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, grp_s);
-    }
-    cp_async_commit();
-  }
+  int pc[4];
+  step_pools(irow, k, 0, t, lane, pc);
+  gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
+  cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
 
   for (int step = 0; step < nsteps; ++step) {
     const bool pass1 = step < ngroups;
     const int grp = pass1 ? step : step - ngroups;
+    const int stage = step & 1;
+    int pf[4] = {-1, -1, -1, -1};
     {
-      const int nx = step + C::NST - 1;
+      const int nx = step + 1;
       if (nx < nsteps) {
-        const int grp_n = nx % ngroups;
-        const int64_t mp = lane < 4 ? bwd_slot_pool(irow, k, grp_n * 4 + lane, t) : -1;
-        bwd_gather<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, grp_n);
+        const int grp_n = nx < ngroups ? nx : nx - ngroups;
+        step_pools(irow, k, grp_n, t, lane, pf);
+        gather_step16<D>(wbase + (nx & 1) * C::STAGE_BYTES, K, V, pf, gl, t, k, grp_n);
       }
       cp_async_commit();
     }
-    const int64_t cur = lane < 4 ? bwd_slot_pool(irow, k, grp * 4 + lane, t) : -1;
-    // validity of this lane's S/dP columns (keys nt*8 + 2qi + e)
+    // visibility of this lane's S/dP columns (keys nt*8 + 2qi + e)
     bool kv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int sig = nt * 2 + (qi >> 1);
-      const int64_t p = __shfl_sync(0xffffffffu, cur, sig);
+      const int pool = (qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2];
+      const int nrows = slot_rows(pool, grp * 4 + sig, k, t);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) kv[nt][e] = p >= 0 && (grp * 4 + sig != k || 4 * p + 2 * (qi & 1) + e <= t);
+      for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
     }
     // tokens of the dK/dV fragment rows this lane adds into: keys g and g+8
     int64_t tok_lo, tok_hi;
     {
-      const int64_t p_lo = __shfl_sync(0xffffffffu, cur, g >> 2);
-      const int64_t p_hi = __shfl_sync(0xffffffffu, cur, 2 + (g >> 2));
-      tok_lo = 4 * p_lo + (g & 3);
-      tok_hi = 4 * p_hi + (g & 3);
-      if (p_lo < 0 || (grp * 4 + (g >> 2) == k && tok_lo > t)) tok_lo = -1;
-      if (p_hi < 0 || (grp * 4 + 2 + (g >> 2) == k && tok_hi > t)) tok_hi = -1;
+      const int slo = g >> 2, row = g & 3;
+      const int p_lo = slo ? pc[1] : pc[0];
+      const int p_hi = slo ? pc[3] : pc[2];
+      tok_lo = row < slot_rows(p_lo, grp * 4 + slo, k, t) ? 4 * (int64_t)p_lo + row : -1;
+      tok_hi = row < slot_rows(p_hi, grp * 4 + 2 + slo, k, t) ? 4 * (int64_t)p_hi + row : -1;
     }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
-    const uint32_t ks_base = wbase + (step % C::NST) * C::STAGE_BYTES;
+    const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
     // S = Q K^T and dP = dO V^T (heads x 16 keys)
@@ -249,6 +207,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 2);
       }
       __syncwarp();
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
       continue;
     }
     // P and scale*dS: bf16 for the dQ product, fp16 for dK/dV (rows g: elements 0,1; rows g+8: 2,3)
@@ -321,6 +281,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       }
     }
     __syncwarp();
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
   }
   cp_async_wait<0>();
 

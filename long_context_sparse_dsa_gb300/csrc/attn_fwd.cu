@@ -18,64 +18,20 @@
 // softmax in registers.  The kernel is bound by the L2->SM gather bandwidth
 // (about 16 flop per gathered byte), not by the MMAs.
 #include "common.cuh"
+#include "gather.cuh"
 #include "launch.h"
 
 namespace dsa {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int KEYS = 16;                    // keys per step (4 pool slots)
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int CHUNKS = D / 8;               // 16-byte chunks per row
-  static constexpr int TILE_BYTES = KEYS * ROW_BYTES;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile + V tile
-  static constexpr int NST = 3;
+  static constexpr int NST = 3;                                  // gather stages per warp
   static constexpr int WARPS = 4;
+  static constexpr int ROW_BYTES = GatherCfg<D>::ROW_BYTES;
+  static constexpr int TILE_BYTES = GatherCfg<D>::TILE_BYTES;
+  static constexpr int STAGE_BYTES = GatherCfg<D>::STAGE_BYTES;
   static constexpr int SMEM = WARPS * NST * STAGE_BYTES;
-  static constexpr int COPIES = 2 * KEYS * CHUNKS / 32;  // 16-byte copies per lane per step
 };
-
-// Pool of slot `slot` for query t, or -1 if the slot holds no visible pool.
-// Slot k is the query's own partial pool.  Bad indices are recorded and skipped.
-__device__ __forceinline__ int64_t slot_pool(const int32_t* irow, int k, int slot, int64_t t) {
-  if (slot < k) {
-    const int64_t p = __ldg(irow + slot);
-    if (p < 0) return -1;
-    if (p >= elig(t)) {
-      record_error(DSA_DEV_ERR_BAD_INDEX);
-      return -1;
-    }
-    return p;
-  }
-  if (slot == k && (t & 3) != 3) return t >> 2;
-  return -1;
-}
-
-template <int D>
-__device__ __forceinline__ void gather_step(uint32_t stage, const __nv_bfloat16* __restrict__ K,
-                                            const __nv_bfloat16* __restrict__ V, int64_t my_pool, int lane,
-                                            int64_t t, int k, int group) {
-  using C = FwdCfg<D>;
-#pragma unroll
-  for (int i = 0; i < C::COPIES; ++i) {
-    const int cid = i * 32 + lane;
-    const int sig = cid / (8 * C::CHUNKS);           // slot within the step
-    const int rem = cid % (8 * C::CHUNKS);
-    const int tensor = rem / (4 * C::CHUNKS);         // 0 = K, 1 = V
-    const int rr = rem % (4 * C::CHUNKS);
-    const int row = rr / C::CHUNKS;
-    const int ch = rr % C::CHUNKS;
-    const int64_t p = __shfl_sync(0xffffffffu, my_pool, sig);
-    const int slot = group * 4 + sig;
-    const int64_t tok = 4 * p + row;
-    const bool valid = p >= 0 && (slot != k || tok <= t);
-    const __nv_bfloat16* base = tensor ? V : K;
-    const __nv_bfloat16* src = base + (valid ? tok * D + ch * 8 : 0);
-    const int key = sig * 4 + row;
-    const uint32_t dst = stage + tensor * C::TILE_BYTES + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4);
-    cp_async16(dst, src, valid ? 16u : 0u);
-  }
-}
 
 template <int D>
 __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
@@ -85,6 +41,7 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
                                                             __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
                                                             int64_t L, int Hq, int k, float scale_log2) {
   using C = FwdCfg<D>;
+  static_assert(C::NST == 3, "the pool ring below is written for three stages");
   extern __shared__ __align__(128) unsigned char fwd_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HG = Hq / 16;
@@ -95,9 +52,9 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
   const int hg = (int)(item % HG);
   const uint32_t wbase = smem_u32(fwd_smem) + warp * C::NST * C::STAGE_BYTES;
   const int32_t* irow = idx + t * k;
-  const int nslots = k + 1;
-  const int ngroups = (nslots + 3) / 4;
+  const int ngroups = (k + 1 + 3) / 4;   // k selected slots + the partial-pool slot
   const int g = lane >> 2, qi = lane & 3;
+  const GatherLane<D> gl = gather_lane<D>(lane);
 
   // Q fragments (A operand, rows = heads hg*16 .. +15).
   uint32_t qa[D / 16][4];
@@ -105,10 +62,11 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
     const uint32_t* q32 = reinterpret_cast<const uint32_t*>(Q + (t * Hq + hg * 16) * D);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      qa[ks][0] = __ldg(q32 + (g * D + ks * 16 + 2 * qi) / 2);
-      qa[ks][1] = __ldg(q32 + ((g + 8) * D + ks * 16 + 2 * qi) / 2);
-      qa[ks][2] = __ldg(q32 + (g * D + ks * 16 + 8 + 2 * qi) / 2);
-      qa[ks][3] = __ldg(q32 + ((g + 8) * D + ks * 16 + 8 + 2 * qi) / 2);
+      const int c0 = (g * D + ks * 16 + 2 * qi) / 2, c1 = ((g + 8) * D + ks * 16 + 2 * qi) / 2;
+      qa[ks][0] = __ldg(q32 + c0);
+      qa[ks][1] = __ldg(q32 + c1);
+      qa[ks][2] = __ldg(q32 + c0 + 4);
+      qa[ks][3] = __ldg(q32 + c1 + 4);
     }
   }
 
@@ -117,42 +75,42 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
   for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-  // prologue
-#pragma unroll
-  for (int s = 0; s < C::NST - 1; ++s) {
-    if (s < ngroups) {
-      const int64_t mp = lane < 4 ? slot_pool(irow, k, s * 4 + lane, t) : -1;
-      gather_step<D>(wbase + s * C::STAGE_BYTES, K, V, mp, lane, t, k, s);
-    }
-    cp_async_commit();
+  // pools of the current step and the next one (steps grp+1, grp+2 are in flight)
+  int pc[4], pn[4];
+  step_pools(irow, k, 0, t, lane, pc);
+  gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
+  cp_async_commit();
+  if (ngroups > 1) {
+    step_pools(irow, k, 1, t, lane, pn);
+    gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl, t, k, 1);
   }
+  cp_async_commit();
 
+  int stage = 0;
   for (int grp = 0; grp < ngroups; ++grp) {
+    int pf[4] = {-1, -1, -1, -1};
     {
-      const int nx = grp + C::NST - 1;
+      const int nx = grp + 2;
       if (nx < ngroups) {
-        const int64_t mp = lane < 4 ? slot_pool(irow, k, nx * 4 + lane, t) : -1;
-        gather_step<D>(wbase + (nx % C::NST) * C::STAGE_BYTES, K, V, mp, lane, t, k, nx);
+        step_pools(irow, k, nx, t, lane, pf);
+        const int st = stage + 2 >= 3 ? stage - 1 : stage + 2;
+        gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl, t, k, nx);
       }
       cp_async_commit();
     }
-    // validity of this lane's four S columns: keys nt*8 + 2*qi + {0,1}
-    const int64_t cur = lane < 4 ? slot_pool(irow, k, grp * 4 + lane, t) : -1;
+    // visibility of this lane's S columns: keys nt*8 + 2*qi + {0,1}
     bool kv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int sig = nt * 2 + (qi >> 1);
-      const int64_t p = __shfl_sync(0xffffffffu, cur, sig);
-      const int slot = grp * 4 + sig;
+      const int pool = (qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2];   // no dynamic register indexing
+      const int nrows = slot_rows(pool, grp * 4 + sig, k, t);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int row = 2 * (qi & 1) + e;
-        kv[nt][e] = p >= 0 && (slot != k || 4 * p + row <= t);
-      }
+      for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
     }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
-    const uint32_t ks_base = wbase + (grp % C::NST) * C::STAGE_BYTES;
+    const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
     float s[2][4];
@@ -224,6 +182,12 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
       }
     }
     __syncwarp();
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      pc[s4] = pn[s4];
+      pn[s4] = pf[s4];
+    }
+    stage = stage == 2 ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 

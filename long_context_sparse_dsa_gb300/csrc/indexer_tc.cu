@@ -17,7 +17,10 @@
 //   * Two accumulators (2 x Hi x 32 columns) let the MMAs of tile i+1 run
 //     while the epilogue drains tile i.
 //   * Warp 0 issues TMA loads (128-byte swizzle): the q_I block of a work unit
-//     (all heads, double-buffered) and a ring of kpool tiles.  Warp 1 allocates
+//     (all heads, double-buffered) and a ring of kpool tiles.  The Hi MMAs of
+//     one k-step share the kpool operand, which is read into the A collector
+//     buffer once and reused (the per-head re-reads would otherwise exceed
+//     the shared-memory bandwidth).  Warp 1 allocates
 //     TMEM and issues the MMAs from one thread; warps 2..9 run the epilogue
 //     (two warps per TMEM lane quarter, each taking 16 of the 32 queries).
 //   * Work unit = (32-query block, up to kSeg pool tiles).  Pool tiles wholly
@@ -201,11 +204,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t adesc = smem_desc_sw128(sA + s * C::A_BYTES + c * C::A_CHUNK + kk * 32);
+              // the Hi MMAs of this k-step share the kpool operand: read it once
+              // into the A collector buffer and reuse it
 #pragma unroll
               for (int h = 0; h < HI; ++h) {
                 const uint64_t bdesc =
                     smem_desc_sw128(sB + bb * C::B_BYTES + (h * C::KC + c) * C::B_CHUNK + kk * 32);
-                tc_mma_f16(d_base + h * C::BN, adesc, bdesc, idesc, (c | kk) != 0);
+                const uint32_t acc = (c | kk) != 0;
+                if (h == 0)
+                  tc_mma_f16_col<kFillA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
+                else if (h == HI - 1)
+                  tc_mma_f16_col<kLastUseA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
+                else
+                  tc_mma_f16_col<kUseA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
               }
             }
           }
@@ -243,24 +254,47 @@ __global__ void __launch_bounds__(320, 1)
         const int ab = acc_iter & 1;
         if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
         tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16;
+        // two batches of HI/2 heads: one TMEM wait per batch, 16 running sums
+        constexpr int HB = HI / 2;
+        const float4* w4 = reinterpret_cast<const float4*>(w_mine);
         float acc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16;
 #pragma unroll
-        for (int h = 0; h < HI; h += 2) {
-          float v0[16], v1[16];
-          tmem_ld16(taddr + h * C::BN, v0);
-          tmem_ld16(taddr + (h + 1) * C::BN, v1);
+        for (int b = 0; b < 2; ++b) {
+          float v[HB][16];
+#pragma unroll
+          for (int h = 0; h < HB; ++h) tmem_ld16(taddr + (b * HB + h) * C::BN, v[h]);
           tmem_ld_wait();
+          if (b == 1) {
+            // the accumulator is in registers: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(ab));
+          }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf(fmaxf(v0[j], 0.f), w_mine[j * HI + h], acc[j]);
+          for (int j = 0; j < 16; ++j) {
+            float wv[HB];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf(fmaxf(v1[j], 0.f), w_mine[j * HI + h + 1], acc[j]);
+            for (int h4 = 0; h4 < HB / 4 + (HB % 4 ? 1 : 0); ++h4) {
+              const float* wp = w_mine + j * HI + b * HB + 4 * h4;
+              if (HB % 4 == 0) {
+                const float4 q4 = *reinterpret_cast<const float4*>(wp);
+                wv[4 * h4 + 0] = q4.x;
+                wv[4 * h4 + 1] = q4.y;
+                wv[4 * h4 + 2] = q4.z;
+                wv[4 * h4 + 3] = q4.w;
+              } else {
+#pragma unroll
+                for (int e = 0; e < HB; ++e) wv[e] = wp[e];
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < HB; ++h) acc[j] = fmaf(fmaxf(v[h][j], 0.f), wv[h], acc[j]);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(ab));
+        (void)w4;
         const int64_t p = tile * C::BM + lane_base + lane;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
