@@ -194,6 +194,32 @@ dsa_status dsa_check_device_error(dsa_stream_t stream);
  * out.  Takes effect for launches enqueued after the call. */
 void dsa_set_wait_limit(uint32_t spins);
 
+/* Size of the fixed device scratch array behind dsa_layer_fwd_noalloc. */
+#define DSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* dsa_layer_fwd without a workspace, for callers that cannot allocate device
+ * memory for the library: for example a plugin inside a host framework whose
+ * own caching allocator owns the device memory and whose operator interface
+ * has no workspace argument, or a code path where a cudaMalloc (which may
+ * synchronise the device) is not allowed.  The paper has no counterpart; it
+ * is an interface convenience.
+ *   Same arguments and outputs as dsa_layer_fwd, minus ws/ws_bytes.  The
+ *   indexer's score block lives in one fixed device array of
+ *   DSA_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU that loads the
+ *   library holds until the process exits; the query chunk is shrunk to
+ *   min(q_chunk, 64 MiB / (4 * L/4)) queries, which does not change any
+ *   result.  A layer whose single score row (L/4 fp32 values) exceeds the
+ *   array returns DSA_ERR_UNSUPPORTED.
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.  Its first
+ *   call on a device looks up the array's device address (once per device,
+ *   with that device current), so make that first call before any stream
+ *   capture.  Every call on a device shares the one array: calls whose work
+ *   overlaps on the GPU (different streams without ordering) race on it.
+ *   Nothing in the array needs to start at zero. */
+dsa_status dsa_layer_fwd_noalloc(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                                 const void *q_idx, const void *k_idx, const float *w,
+                                 void *o, float *lse, int32_t *idx, void *kpool, dsa_stream_t stream);
+
 /* Test hook for the failure-detection path: enqueue a one-CTA kernel that
  * waits on an mbarrier nothing arrives on.  The bounded wait gives up after
  * `spins` polls (1 .. 2^24) and records a timeout; the kernel then returns

@@ -8,7 +8,8 @@ or no GPU is present, calls raise.
 
 Entry points (same names as the C ABI, without the ``dsa_`` prefix):
 pool_keys, indexer_score, topk, sparse_attn_fwd, sparse_attn_bwd,
-layer_fwd, layer_bwd, check_device_error, workspace_bytes, validate_dims.
+layer_fwd, layer_bwd, check_device_error, workspace_bytes, validate_dims,
+layer_fwd_noalloc.
 """
 from __future__ import annotations
 
@@ -68,6 +69,7 @@ def _load():
             "dsa_sparse_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_layer_fwd_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
             "dsa_selftest_bounded_wait": ([u32, P], ctypes.c_int),
@@ -160,6 +162,13 @@ def layer_fwd(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, ws, ws_bytes=N
     _check(_load().dsa_layer_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(w),
                                  _ptr(o), _ptr(lse), _ptr(idx), _ptr(kpool), _ptr(ws), int(ws_bytes),
                                  _stream(stream)), "dsa_layer_fwd")
+
+
+def layer_fwd_noalloc(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, stream=None):
+    """dsa_layer_fwd with the score block in the library's fixed device array (no workspace)."""
+    _check(_load().dsa_layer_fwd_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx),
+                                         _ptr(w), _ptr(o), _ptr(lse), _ptr(idx), _ptr(kpool), _stream(stream)),
+           "dsa_layer_fwd_noalloc")
 
 
 def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=0, stream=None):

@@ -140,6 +140,12 @@ dsa_status do_bwd(const dsa_dims* d, const void* q, const void* k, const void* v
 
 }  // namespace
 
+namespace dsa {
+// Lets entry points defined in other files of the library report a detail
+// through dsa_last_error_message.
+void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+}  // namespace dsa
+
 extern "C" {
 
 const char* dsa_status_string(dsa_status st) {
