@@ -165,12 +165,13 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
-    // S = Q K^T and dP = dO V^T (heads x 16 keys)
-    float s[2][4], dp[2][4];
+    // S = Q K^T and dP = dO V^T (heads x 16 keys), each as two independent
+    // accumulation chains (even / odd k-steps)
+    float s[2][4], dp[2][4], s2[2][4], dp2[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = dp[nt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) s[nt][e] = dp[nt][e] = s2[nt][e] = dp2[nt][e] = 0.f;
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int key = (mtx >> 1) * 8 + r;
@@ -178,26 +179,40 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       for (int ks = 0; ks < D / 16; ++ks) {
         const int ch = 2 * ks + (mtx & 1);
         const uint32_t off = key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
+        uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
         ldsm_x4(ks_base + off, b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-        ldsm_x4(vs_base + off, b0, b1, b2, b3);
-        mma_bf16_16816(dp[0], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b0, b1);
-        mma_bf16_16816(dp[1], da[ks][0], da[ks][1], da[ks][2], da[ks][3], b2, b3);
+        ldsm_x4(vs_base + off, c0, c1, c2, c3);
+        if (ks & 1) {
+          mma_bf16_16816(s2[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(s2[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          mma_bf16_16816(dp2[0], da[ks][0], da[ks][1], da[ks][2], da[ks][3], c0, c1);
+          mma_bf16_16816(dp2[1], da[ks][0], da[ks][1], da[ks][2], da[ks][3], c2, c3);
+        } else {
+          mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          mma_bf16_16816(dp[0], da[ks][0], da[ks][1], da[ks][2], da[ks][3], c0, c1);
+          mma_bf16_16816(dp[1], da[ks][0], da[ks][1], da[ks][2], da[ks][3], c2, c3);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s[nt][e] += s2[nt][e];
+          dp[nt][e] += dp2[nt][e];
+        }
     }
     if (pass1) {
       // D partial sums over this lane's columns: rows g and g+8
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         if (kv[nt][0]) {
-          Dg = fmaf(exp2f(s[nt][0] * scale_log2 - lse_g), dp[nt][0], Dg);
-          Dg8 = fmaf(exp2f(s[nt][2] * scale_log2 - lse_g8), dp[nt][2], Dg8);
+          Dg = fmaf(ex2_approx(s[nt][0] * scale_log2 - lse_g), dp[nt][0], Dg);
+          Dg8 = fmaf(ex2_approx(s[nt][2] * scale_log2 - lse_g8), dp[nt][2], Dg8);
         }
         if (kv[nt][1]) {
-          Dg = fmaf(exp2f(s[nt][1] * scale_log2 - lse_g), dp[nt][1], Dg);
-          Dg8 = fmaf(exp2f(s[nt][3] * scale_log2 - lse_g8), dp[nt][3], Dg8);
+          Dg = fmaf(ex2_approx(s[nt][1] * scale_log2 - lse_g), dp[nt][1], Dg);
+          Dg8 = fmaf(ex2_approx(s[nt][3] * scale_log2 - lse_g8), dp[nt][3], Dg8);
         }
       }
       if (step == ngroups - 1) {
@@ -215,10 +230,10 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     uint32_t pp[2][2], dd[2][2], dh[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float p0 = kv[nt][0] ? exp2f(s[nt][0] * scale_log2 - lse_g) : 0.f;
-      const float p1 = kv[nt][1] ? exp2f(s[nt][1] * scale_log2 - lse_g) : 0.f;
-      const float p2 = kv[nt][0] ? exp2f(s[nt][2] * scale_log2 - lse_g8) : 0.f;
-      const float p3 = kv[nt][1] ? exp2f(s[nt][3] * scale_log2 - lse_g8) : 0.f;
+      const float p0 = kv[nt][0] ? ex2_approx(s[nt][0] * scale_log2 - lse_g) : 0.f;
+      const float p1 = kv[nt][1] ? ex2_approx(s[nt][1] * scale_log2 - lse_g) : 0.f;
+      const float p2 = kv[nt][0] ? ex2_approx(s[nt][2] * scale_log2 - lse_g8) : 0.f;
+      const float p3 = kv[nt][1] ? ex2_approx(s[nt][3] * scale_log2 - lse_g8) : 0.f;
       const float s0 = scale * p0 * (dp[nt][0] - Dg), s1 = scale * p1 * (dp[nt][1] - Dg);
       const float s2 = scale * p2 * (dp[nt][2] - Dg8), s3 = scale * p3 * (dp[nt][3] - Dg8);
       pp[nt][0] = pack_f16(p0, p1);

@@ -113,9 +113,13 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
     const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
-    float s[2][4];
+    // S = Q K^T as four independent accumulation chains (two per key octet,
+    // even and odd k-steps) so consecutive MMAs do not wait on each other
+    float s[2][4], s2[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int key = (mtx >> 1) * 8 + r;
@@ -124,9 +128,18 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
         const int ch = 2 * ks + (mtx & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        if (ks & 1) {
+          mma_bf16_16816(s2[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(s2[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        } else {
+          mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     }
     // online softmax (log2 domain); c0,c1 -> head g, c2,c3 -> head g+8
     float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -145,27 +158,31 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
+    const float a0 = ex2_approx(m0 - base0), a1 = ex2_approx(m1 - base1);
     m0 = mn0;
     m1 = mn1;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - base0);
-      s[nt][1] = exp2f(s[nt][1] - base0);
-      s[nt][2] = exp2f(s[nt][2] - base1);
-      s[nt][3] = exp2f(s[nt][3] - base1);
+      s[nt][0] = ex2_approx(s[nt][0] - base0);
+      s[nt][1] = ex2_approx(s[nt][1] - base0);
+      s[nt][2] = ex2_approx(s[nt][2] - base1);
+      s[nt][3] = ex2_approx(s[nt][3] - base1);
       rs0 += s[nt][0] + s[nt][1];
       rs1 += s[nt][2] + s[nt][3];
     }
     l0 = l0 * a0 + rs0;
     l1 = l1 * a1 + rs1;
+    // rescale O only when some row's running max moved (a == 1 otherwise, and
+    // multiplying by 1 is exact, so skipping changes nothing)
+    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= a0;
-      o[n][1] *= a0;
-      o[n][2] *= a1;
-      o[n][3] *= a1;
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= a0;
+        o[n][1] *= a0;
+        o[n][2] *= a1;
+        o[n][3] *= a1;
+      }
     }
     const uint32_t pa0 = pack_bf16(s[0][0], s[0][1]), pa1 = pack_bf16(s[0][2], s[0][3]);
     const uint32_t pa2 = pack_bf16(s[1][0], s[1][1]), pa3 = pack_bf16(s[1][2], s[1][3]);
