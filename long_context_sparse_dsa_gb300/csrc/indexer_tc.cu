@@ -8,19 +8,18 @@
 //   s[t,p] = sum_h w[t,h] * max(0, q_I[t,h,:] . kpool[p,:]),   p < elig(t).
 //
 // Design (one persistent CTA per SM, warp-specialised):
-//   * MMA shape M=128 pools x N=32 queries x K=16, one MMA per indexer head:
-//     D_h[p,t] = kpool[p,:] . q_I[t,h,:], fp32 accumulators in tensor memory.
-//     The Hi heads of one 32-query block sit side by side in TMEM columns
-//     (h*32 + t), so an epilogue thread -- which owns one pool (TMEM lane) --
-//     finds all heads of a query in its own registers and applies ReLU, the
-//     head weight and the head sum without any cross-thread exchange.
+//   * MMA shape M=128 pools x N=32*Hi x K=16.  The Hi heads of a 32-query
+//     block are Hi*32 consecutive rows of q_I ([L, Hi, di] row-major), so one
+//     MMA computes D[p, t*Hi+h] = kpool[p,:] . q_I[t,h,:] for all heads at
+//     once (N = 256 at Hi = 8), with fp32 accumulators in tensor memory.  An
+//     epilogue thread owns one pool (TMEM lane) and finds the Hi heads of a
+//     query in adjacent columns of its own registers, so ReLU, the head weight
+//     and the head sum need no cross-thread exchange.
 //   * Two accumulators (2 x Hi x 32 columns) let the MMAs of tile i+1 run
 //     while the epilogue drains tile i.
 //   * Warp 0 issues TMA loads (128-byte swizzle): the q_I block of a work unit
-//     (all heads, double-buffered) and a ring of kpool tiles.  The Hi MMAs of
-//     one k-step share the kpool operand, which is read into the A collector
-//     buffer once and reused (the per-head re-reads would otherwise exceed
-//     the shared-memory bandwidth).  Warp 1 allocates
+//     (one box of 32*Hi rows per 64-wide K chunk, double-buffered) and a ring
+//     of kpool tiles.  Warp 1 allocates
 //     TMEM and issues the MMAs from one thread; warps 2..9 run the epilogue
 //     (two warps per TMEM lane quarter, each taking 16 of the 32 queries).
 //   * Work unit = (32-query block, up to kSeg pool tiles).  Pool tiles wholly
@@ -43,9 +42,10 @@ struct IdxCfg {
   static constexpr int BN = 32;                       // queries per block (MMA N)
   static constexpr int KC = DI / 64;                  // 128-byte K chunks
   static constexpr int A_CHUNK = BM * 128;            // bytes of one K chunk of a kpool tile
-  static constexpr int B_CHUNK = BN * 128;            // bytes of one (head, K chunk) of a q_I block
+  static constexpr int NCOL = BN * HI;                 // MMA N: 32 queries x Hi heads
+  static constexpr int B_CHUNK = NCOL * 128;          // bytes of one K chunk of a q_I block
   static constexpr int A_BYTES = KC * A_CHUNK;
-  static constexpr int B_BYTES = HI * KC * B_CHUNK;
+  static constexpr int B_BYTES = KC * B_CHUNK;
   static constexpr int NSA = DI == 64 ? 4 : 2;        // kpool tile stages
   static constexpr int ACC_COLS = HI * BN;            // TMEM columns per accumulator
   static constexpr int TMEM_COLS = 2 * ACC_COLS;      // 256 or 512 (power of two)
@@ -160,10 +160,8 @@ __global__ void __launch_bounds__(320, 1)
         const int bb = b_iter & 1;
         if (!(ok = mbar_wait(empty_b(bb), ((b_iter >> 1) & 1) ^ 1, abort_flag))) break;
         mbar_arrive_expect_tx(full_b(bb), C::B_BYTES);
-        for (int h = 0; h < HI; ++h)
-          for (int c = 0; c < C::KC; ++c)
-            tma_load_3d(sB + bb * C::B_BYTES + (h * C::KC + c) * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, h,
-                        (int32_t)it.t0);
+        for (int c = 0; c < C::KC; ++c)
+          tma_load_2d(sB + bb * C::B_BYTES + c * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, (int32_t)(it.t0 * HI));
         ++b_iter;
         for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
           const int s = a_iter % C::NSA;
@@ -186,7 +184,7 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::NCOL);
       uint32_t a_iter = 0, b_iter = 0, acc_iter = 0;
       bool ok = true;
       while (ok && it.next<C::BN, C::BM, C::SEG>()) {
@@ -204,20 +202,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t adesc = smem_desc_sw128(sA + s * C::A_BYTES + c * C::A_CHUNK + kk * 32);
-              // the Hi MMAs of this k-step share the kpool operand: read it once
-              // into the A collector buffer and reuse it
-#pragma unroll
-              for (int h = 0; h < HI; ++h) {
-                const uint64_t bdesc =
-                    smem_desc_sw128(sB + bb * C::B_BYTES + (h * C::KC + c) * C::B_CHUNK + kk * 32);
-                const uint32_t acc = (c | kk) != 0;
-                if (h == 0)
-                  tc_mma_f16_col<kFillA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
-                else if (h == HI - 1)
-                  tc_mma_f16_col<kLastUseA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
-                else
-                  tc_mma_f16_col<kUseA>(d_base + h * C::BN, adesc, bdesc, idesc, acc);
-              }
+              const uint64_t bdesc = smem_desc_sw128(sB + bb * C::B_BYTES + c * C::B_CHUNK + kk * 32);
+              tc_mma_f16(d_base, adesc, bdesc, idesc, (c | kk) != 0);
             }
           }
           tc_commit(empty_a(s));
@@ -254,47 +240,42 @@ __global__ void __launch_bounds__(320, 1)
         const int ab = acc_iter & 1;
         if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16;
-        // two batches of HI/2 heads: one TMEM wait per batch, 16 running sums
-        constexpr int HB = HI / 2;
-        const float4* w4 = reinterpret_cast<const float4*>(w_mine);
+        // this thread: pool (lane_base + lane), queries half*16 .. +15, columns
+        // (query*Hi + head); batches of 64 columns = 64/Hi queries
+        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16 * HI;
+        constexpr int NB = 16 * HI / 64;
+        constexpr int QB = 64 / HI;                // queries per batch
         float acc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] = 0.f;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          float v[HB][16];
+        for (int b = 0; b < NB; ++b) {
+          float v[4][16];
 #pragma unroll
-          for (int h = 0; h < HB; ++h) tmem_ld16(taddr + (b * HB + h) * C::BN, v[h]);
+          for (int i = 0; i < 4; ++i) tmem_ld16(taddr + b * 64 + i * 16, v[i]);
           tmem_ld_wait();
-          if (b == 1) {
+          if (b == NB - 1) {
             // the accumulator is in registers: hand it back to the MMA warp
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(ab));
           }
+          // weights of this batch's queries, 4 per shared-memory load (broadcast)
+          float wv[64];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float wv[HB];
+          for (int i4 = 0; i4 < 16; ++i4) {
+            const float4 q4 = reinterpret_cast<const float4*>(w_mine + b * 64)[i4];
+            wv[4 * i4 + 0] = q4.x;
+            wv[4 * i4 + 1] = q4.y;
+            wv[4 * i4 + 2] = q4.z;
+            wv[4 * i4 + 3] = q4.w;
+          }
 #pragma unroll
-            for (int h4 = 0; h4 < HB / 4 + (HB % 4 ? 1 : 0); ++h4) {
-              const float* wp = w_mine + j * HI + b * HB + 4 * h4;
-              if (HB % 4 == 0) {
-                const float4 q4 = *reinterpret_cast<const float4*>(wp);
-                wv[4 * h4 + 0] = q4.x;
-                wv[4 * h4 + 1] = q4.y;
-                wv[4 * h4 + 2] = q4.z;
-                wv[4 * h4 + 3] = q4.w;
-              } else {
-#pragma unroll
-                for (int e = 0; e < HB; ++e) wv[e] = wp[e];
-              }
-            }
-#pragma unroll
-            for (int h = 0; h < HB; ++h) acc[j] = fmaf(fmaxf(v[h][j], 0.f), wv[h], acc[j]);
+          for (int c = 0; c < 64; ++c) {
+            const int jl = b * QB + c / HI;         // heads of one query in order 0..Hi-1
+            acc[jl] = fmaf(fmaxf(v[c / 16][c % 16], 0.f), wv[c], acc[jl]);
           }
         }
-        (void)w4;
         const int64_t p = tile * C::BM + lane_base + lane;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -338,11 +319,11 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tq, tk;
   {
-    const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)HI, (cuuint64_t)L};
-    const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)HI * DI * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)C::BN};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides, box, estr,
+    const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)L * HI};
+    const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)C::NCOL};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_idx), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
