@@ -190,7 +190,8 @@ dsa_status dsa_layer_bwd(const dsa_dims *dims, const void *q, const void *k, con
 dsa_status dsa_check_device_error(dsa_stream_t stream);
 
 /* Test hook: the number of spin iterations after which a bounded device-side
- * wait gives up (default 1<<20, about a second at most).  Lowering it lets a test make a wait run
+ * wait gives up (default 1<<20).  Independently of this, every device wait
+ * gives up after 2 s of wall time.  Lowering it lets a test make a wait run
  * out.  Takes effect for launches enqueued after the call. */
 void dsa_set_wait_limit(uint32_t spins);
 

@@ -44,24 +44,44 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// One poll of the phase with the given parity.  The thread may be suspended
+// while it waits, for at most kSuspendHintNs nanoseconds per poll.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity.  Returns false (and
-// records a timeout) if `limit` polls pass or *abort becomes non-zero.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Upper bound on any single device-side wait, in nanoseconds of wall time.
+constexpr uint64_t kWaitDeadlineNs = 2000000000ull;
+// Bounded wait for the phase with the given parity.  Gives up (returns false
+// and records a timeout) after `limit` polls or kWaitDeadlineNs of wall time,
+// whichever comes first, or returns false early once *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait_n(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                             uint32_t limit) {
+  uint64_t t0 = 0;
   for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (abort_flag && (i & 63u) == 63u && *abort_flag) return false;
+    if ((i & 15u) == 15u) {
+      if (abort_flag && *abort_flag) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitDeadlineNs) {
+        break;
+      }
+    }
   }
   record_error(DSA_DEV_ERR_TIMEOUT);
   if (abort_flag) *abort_flag = 1;

@@ -47,6 +47,7 @@ struct IdxCfg {
   static constexpr int A_BYTES = KC * A_CHUNK;
   static constexpr int B_BYTES = KC * B_CHUNK;
   static constexpr int NSA = DI == 64 ? 4 : 2;        // kpool tile stages
+  static_assert(NSA <= 4, "the barrier slots below hold at most four kpool stages");
   static constexpr int ACC_COLS = HI * BN;            // TMEM columns per accumulator
   static constexpr int TMEM_COLS = 2 * ACC_COLS;      // 256 or 512 (power of two)
   static constexpr int SEG = 16;                      // pool tiles per work unit
@@ -280,7 +281,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int64_t t = it.t0 + half * 16 + j;
-          if (t < q_end && p < elig(t)) scores[(t - q_begin) * P + p] = acc[j];
+          // streaming store: the score block is read once, by the top-k
+          if (t < q_end && p < elig(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
         }
         ++acc_iter;
       }

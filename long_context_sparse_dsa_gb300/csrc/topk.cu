@@ -13,22 +13,34 @@
 // and padded with -1; the result depends only on the scores (no atomics
 // decide order), so it is bitwise reproducible.
 //
-// One CTA of kTopkThreads threads per row.  Global traffic is two passes
-// over the row: pass 1 builds the top-11-bit histogram; pass 2 copies every
-// key in the threshold bin or above (at most k-1 + that bin) with its index,
-// in index order, into shared memory; the remaining rounds and the selection
-// run there.  Rows up to kRowCap scores are also staged in shared memory in
-// pass 1, so pass 2 reads SMEM.  Tie-heavy rows whose threshold bin overflows
-// the candidate buffer fall back to rounds and selection over the row.
+// One CTA of kTopkThreads threads per row, one read of the row in the
+// common case:
+//   1. 1024 evenly spaced samples give a threshold tau: the r-th largest
+//      sample, r = mu + 4 sqrt(mu) + 2 with mu = k * 1024 / n the expected
+//      number of samples at or above the k-th score, so that tau lies below
+//      the k-th score with high probability while few scores pass it (rows of
+//      at most kCandCap scores skip this and keep every score);
+//   2. one pass over the row copies every score >= tau, with its index, into
+//      shared memory; each warp compacts its own contiguous segment in index
+//      order, so the candidates come out in ascending pool order with no
+//      block-wide scan;
+//   3. the exact radix select and the ordered selection run on those
+//      candidates.
+// If the candidates number fewer than k (tau too high) or overflow the
+// buffer (tie-heavy rows), the row falls back to the exact two-pass path:
+// a histogram pass, then an ordered compaction of the threshold bin and
+// above, or -- when even that overflows -- rounds and selection over the
+// whole row.
 #include "common.cuh"
 #include "launch.h"
 
 namespace dsa {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kRowCap = 12288;   // scores staged in SMEM (48 KB)
-constexpr int kCandCap = 6144;   // candidate keys + indices kept in SMEM (48 KB)
+constexpr int kCandCap = 4096;                        // candidate keys + indices in SMEM (32 KB)
+constexpr int kWarpCap = kCandCap / kTopkWarps;       // per-warp compaction region
+constexpr int kSamples = 1024;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -74,7 +86,7 @@ __device__ __forceinline__ void hist_add(int* hist, int bin) {
 // Find, scanning bins from the top, the bin where the running count reaches
 // `need`.  Writes the bin and the count strictly above it to sel[0], sel[1].
 __device__ __forceinline__ void find_bin(const int* hist, int nbins, int need, int* warp_buf, int* sel) {
-  const int per = (nbins + kTopkThreads - 1) / kTopkThreads;  // 4 or 2
+  const int per = (nbins + kTopkThreads - 1) / kTopkThreads;
   int local = 0;
   for (int j = 0; j < per; ++j) {
     const int b = nbins - 1 - (threadIdx.x * per + j);
@@ -93,6 +105,41 @@ __device__ __forceinline__ void find_bin(const int* hist, int nbins, int need, i
     cum += h;
   }
   __syncthreads();
+}
+
+// Exact `need`-th largest key among keys[0..m) (need <= m): three radix
+// rounds.  Returns the key T; *above = how many keys are > T.
+__device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int need, int* hist, int* warp_buf,
+                                               int* sel, int* above) {
+  const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+  uint32_t prefix = 0;
+  int got_above = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+#pragma unroll
+  for (int round = 0; round < 3; ++round) {
+    const int nb = 1 << widths[round];
+    for (int b = threadIdx.x; b < nb; b += kTopkThreads) hist[b] = 0;
+    __syncthreads();
+    const int sh = shifts[round];
+    const int hi = sh + widths[round];   // bits above this digit must equal the prefix
+    for (int i = threadIdx.x; i < m_round; i += kTopkThreads) {
+      int bin = -1;
+      if (i < m) {
+        const uint32_t key = keys[i];
+        const bool match = hi >= 32 ? true : ((key >> hi) == prefix);
+        if (match) bin = (int)((key >> sh) & (uint32_t)(nb - 1));
+      }
+      hist_add(hist, bin);
+    }
+    __syncthreads();
+    find_bin(hist, nb, need, warp_buf, sel);
+    prefix = (prefix << widths[round]) | (uint32_t)sel[0];
+    need -= sel[1];
+    got_above += sel[1];
+  }
+  *above = got_above;
+  return prefix;
 }
 
 // One tile of the ordered selection: keep keys > T and the first `need_eq`
@@ -127,18 +174,35 @@ __device__ __forceinline__ void select_tile(const uint32_t (&kk)[4], int base, i
   taken += take_total;
 }
 
-template <bool STAGE>
+// Ordered selection of the top k over candidates (keys, ids) in index order.
+__device__ __forceinline__ void select_from_candidates(const uint32_t* cand_key, const int32_t* cand_idx, int m,
+                                                       int k, int* hist, int* warp_buf, int* sel, int32_t* out) {
+  int above;
+  const uint32_t T = select_kth(cand_key, m, k, hist, warp_buf, sel, &above);
+  const int need_eq = k - above;
+  const int c_round = (m + 4 * kTopkThreads - 1) / (4 * kTopkThreads) * (4 * kTopkThreads);
+  int eq_seen = 0, taken = 0;
+  for (int base = threadIdx.x * 4; base < c_round && taken < k; base += 4 * kTopkThreads) {
+    uint32_t kk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) kk[j] = (base + j < m) ? cand_key[base + j] : 0u;
+    select_tile(kk, base, m, T, need_eq, eq_seen, taken, warp_buf, cand_idx, out);
+  }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
                                                             int64_t q_begin, int64_t q_count,
                                                             int32_t* __restrict__ idx) {
-  extern __shared__ __align__(16) unsigned char topk_smem[];
-  int* hist = reinterpret_cast<int*>(topk_smem);                     // [2048]
-  int* warp_buf = hist + 2048;                                       // [32]
-  int* sel = warp_buf + 32;                                          // [4]
-  uint32_t* cand_key = reinterpret_cast<uint32_t*>(sel + 4);         // [kCandCap]
-  int32_t* cand_idx = reinterpret_cast<int32_t*>(cand_key + kCandCap);  // [kCandCap]
-  uint32_t* row_keys = reinterpret_cast<uint32_t*>(cand_idx + kCandCap);  // [kRowCap] when STAGE
+  __shared__ int hist[2048];
+  __shared__ int warp_buf[32];
+  __shared__ int sel[4];
+  __shared__ int warp_cnt[kTopkWarps];
+  __shared__ int flag_overflow;
+  __shared__ __align__(16) uint32_t cand_key[kCandCap];
+  __shared__ __align__(16) int32_t cand_idx[kCandCap];
+  __shared__ uint32_t samples[kSamples];
 
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   // Longer rows (later queries) first.
   const int64_t r = q_count - 1 - (int64_t)blockIdx.x;
   const int64_t t = q_begin + r;
@@ -151,30 +215,110 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const int n = (int)n64;
   const float* row = scores + r * P;
   const bool vec4 = ((P & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15) == 0);
-  const int n_round = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads) * (4 * kTopkThreads);
 
-  // Four consecutive keys of the row starting at `base` (0 past the end).
-  auto load4 = [&](int base, uint32_t (&kk)[4]) {
-    if (STAGE) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) kk[j] = (base + j < n) ? row_keys[base + j] : 0u;
-    } else if (vec4 && base + 3 < n) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + base));
+  // ---- 1. threshold from evenly spaced samples ------------------------------
+  uint32_t tau = 0u;   // every key is >= 0
+  if (n > kCandCap) {
+    for (int i = threadIdx.x; i < kSamples; i += kTopkThreads)
+      samples[i] = order_key(__ldg(row + (int)(((int64_t)i * n) / kSamples)));
+    __syncthreads();
+    // mu = expected samples at or above the true k-th score; take 4 sigma more
+    const float mu = (float)k * (float)kSamples / (float)n;
+    int rank = (int)(mu + 4.f * sqrtf(mu)) + 2;
+    if (rank > kSamples) rank = kSamples;
+    int above_s;
+    tau = select_kth(samples, kSamples, rank, hist, warp_buf, sel, &above_s);
+  }
+
+  // ---- 2. one pass: warp-segmented ordered compaction of keys >= tau -------
+  if (threadIdx.x == 0) flag_overflow = 0;
+  const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 127) & ~127;   // multiple of 128 elements
+  const int w_begin = wid * seg;
+  const int w_end = min(n, w_begin + seg);
+  int wcount = 0;
+  bool overflow = false;
+  uint32_t* my_key = cand_key + wid * kWarpCap;
+  int32_t* my_idx = cand_idx + wid * kWarpCap;
+  for (int base = w_begin; base < w_end; base += 128) {
+    const int e = base + 4 * lane;
+    uint32_t kk[4];
+    if (vec4 && e + 3 < w_end) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + e));
       kk[0] = order_key(f.x);
       kk[1] = order_key(f.y);
       kk[2] = order_key(f.z);
       kk[3] = order_key(f.w);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kk[j] = (base + j < n) ? order_key(__ldg(row + base + j)) : 0u;
+      for (int j = 0; j < 4; ++j) kk[j] = (e + j < w_end) ? order_key(__ldg(row + e + j)) : 0u;
     }
-  };
-
-  // ---- pass 1: histogram of the top 11 bits (and stage the row) -------------
-  for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
+    bool f[4];
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[j] = (e + j < w_end) && kk[j] >= tau;
+      c += f[j];
+    }
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (wcount + tot > kWarpCap) {
+      overflow = true;
+      break;
+    }
+    int pos = wcount + incl - c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (f[j]) {
+        my_key[pos] = kk[j];
+        my_idx[pos] = e + j;
+        ++pos;
+      }
+    wcount += tot;
+  }
+  if (lane == 0) {
+    warp_cnt[wid] = wcount;
+    if (overflow) flag_overflow = 1;
+  }
   __syncthreads();
-  for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
-    uint32_t kk[4];
+  int m = 0;
+  for (int w = 0; w < kTopkWarps; ++w) m += warp_cnt[w];
+  const bool fast = !flag_overflow && m >= k;
+  if (fast) {
+    // close the gaps between the warp regions (in warp order = index order)
+    int dst = 0;
+    for (int w = 0; w < kTopkWarps; ++w) {
+      const int cnt = warp_cnt[w];
+      const int src = w * kWarpCap;
+      // src >= dst always; copy forward in chunks so overlapping moves stay correct
+      for (int i0 = 0; i0 < cnt; i0 += kTopkThreads) {
+        const int i = i0 + threadIdx.x;
+        uint32_t kv = 0;
+        int32_t iv = 0;
+        if (i < cnt) {
+          kv = cand_key[src + i];
+          iv = cand_idx[src + i];
+        }
+        __syncthreads();
+        if (i < cnt) {
+          cand_key[dst + i] = kv;
+          cand_idx[dst + i] = iv;
+        }
+        __syncthreads();
+      }
+      dst += cnt;
+    }
+    select_from_candidates(cand_key, cand_idx, m, k, hist, warp_buf, sel, out);
+    return;
+  }
+
+  // ---- fallback: histogram pass, then the threshold bin and above ---------
+  const int n_round = (n + 4 * kTopkThreads - 1) / (4 * kTopkThreads) * (4 * kTopkThreads);
+  auto load4 = [&](int base, uint32_t (&kk)[4]) {
     if (vec4 && base + 3 < n) {
       const float4 f = __ldg(reinterpret_cast<const float4*>(row + base));
       kk[0] = order_key(f.x);
@@ -185,23 +329,21 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 #pragma unroll
       for (int j = 0; j < 4; ++j) kk[j] = (base + j < n) ? order_key(__ldg(row + base + j)) : 0u;
     }
+  };
+  for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
+  __syncthreads();
+  for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
+    uint32_t kk[4];
+    load4(base, kk);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool valid = base + j < n;
-      if (STAGE && valid) row_keys[base + j] = kk[j];
-      hist_add(hist, valid ? (int)(kk[j] >> 21) : -1);
-    }
+    for (int j = 0; j < 4; ++j) hist_add(hist, base + j < n ? (int)(kk[j] >> 21) : -1);
   }
   __syncthreads();
   find_bin(hist, 2048, k, warp_buf, sel);
   const uint32_t b0 = (uint32_t)sel[0];
-  const int above0 = sel[1];
-  const int need1 = k - above0;
-  const int n_cand = above0 + hist[b0];
+  const int n_cand = sel[1] + hist[b0];
   __syncthreads();
-
   if (n_cand <= kCandCap) {
-    // ---- pass 2: ordered compaction of every key in bins >= b0 -------------
     int written = 0;
     for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
       uint32_t kk[4];
@@ -225,43 +367,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
       written += tot;
     }
     __syncthreads();
-    // ---- rounds 1 and 2 on the candidates ------------------------------------
-    for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
-    __syncthreads();
-    const int m_round = (n_cand + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-    for (int i = threadIdx.x; i < m_round; i += kTopkThreads) {
-      int bin = -1;
-      if (i < n_cand && (cand_key[i] >> 21) == b0) bin = (int)((cand_key[i] >> 10) & 0x7FFu);
-      hist_add(hist, bin);
-    }
-    __syncthreads();
-    find_bin(hist, 2048, need1, warp_buf, sel);
-    const uint32_t pre1 = (b0 << 11) | (uint32_t)sel[0];
-    const int need2 = need1 - sel[1];
-    for (int b = threadIdx.x; b < 1024; b += kTopkThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < m_round; i += kTopkThreads) {
-      int bin = -1;
-      if (i < n_cand && (cand_key[i] >> 10) == pre1) bin = (int)(cand_key[i] & 0x3FFu);
-      hist_add(hist, bin);
-    }
-    __syncthreads();
-    find_bin(hist, 1024, need2, warp_buf, sel);
-    const uint32_t T = (pre1 << 10) | (uint32_t)sel[0];
-    const int need_eq = need2 - sel[1];
-    // ---- ordered selection over the candidates (already in index order) -----
-    const int c_round = (n_cand + 4 * kTopkThreads - 1) / (4 * kTopkThreads) * (4 * kTopkThreads);
-    int eq_seen = 0, taken = 0;
-    for (int base = threadIdx.x * 4; base < c_round && taken < k; base += 4 * kTopkThreads) {
-      uint32_t kk[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) kk[j] = (base + j < n_cand) ? cand_key[base + j] : 0u;
-      select_tile(kk, base, n_cand, T, need_eq, eq_seen, taken, warp_buf, cand_idx, out);
-    }
+    select_from_candidates(cand_key, cand_idx, n_cand, k, hist, warp_buf, sel, out);
     return;
   }
-
-  // ---- fallback (tie-heavy rows): refine over the row, select over the row --
+  // tie-heavy: rounds 1 and 2 over the row, then the ordered selection over the row
+  const int need1 = k - sel[1];
   for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
   __syncthreads();
   for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
@@ -299,19 +409,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 cudaError_t launch_topk(int64_t L, int k, const float* scores, int64_t q_begin, int64_t q_count, int32_t* idx,
                         cudaStream_t s) {
   const int64_t P = L / 4;
-  const int64_t max_elig = (q_begin + q_count) / 4;
-  const size_t base_smem = (2048 + 32 + 4) * sizeof(int) + (size_t)kCandCap * 8;
-  if (max_elig <= kRowCap) {
-    const size_t smem = base_smem + (size_t)kRowCap * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<true><<<(unsigned)q_count, kTopkThreads, smem, s>>>(scores, P, k, q_begin, q_count, idx);
-  } else {
-    cudaError_t e =
-        cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)base_smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<false><<<(unsigned)q_count, kTopkThreads, base_smem, s>>>(scores, P, k, q_begin, q_count, idx);
-  }
+  topk_kernel<<<(unsigned)q_count, kTopkThreads, 0, s>>>(scores, P, k, q_begin, q_count, idx);
   return cudaGetLastError();
 }
 
