@@ -8,7 +8,7 @@
 //
 // Everything that depends only on the lane is computed once (GatherLane);
 // per step a lane needs the 4 pool indices of the step (one 32-bit shuffle
-// each) and issues its copies with a single address add per copy.  Keys that
+// each), one address per pool slot, and then one compare per copy.  Keys that
 // are not visible (empty slot, or tokens after t in the partial pool) are
 // zero-filled.
 #pragma once
@@ -28,18 +28,35 @@ struct GatherCfg {
   static constexpr int ROWS_PER_COPY = 32 / CHUNKS;     // rows covered by one copy instruction (2 or 4)
 };
 
-// Copy i of a lane covers: slot sig(i), tensor ten(i), row = row_base(i) + lane / CHUNKS, chunk = lane % CHUNKS.
+// Lane constants of the gather.  Copy (sig, ten, rb) of a lane moves the
+// 16-byte chunk `ch` of row  rb*ROWS_PER_COPY + row_lo  of slot sig, tensor
+// ten (0 = K, 1 = V).  Within the step's shared tile that row is key
+// sig*4 + row and its chunk lands at position ch ^ (key & 7); since key & 7 =
+// (sig & 1)*4 + row, the destination offset depends on the lane only through
+// dst_off[sig & 1][rb] (the sig*4 rows and the tensor add compile-time
+// constants).
 template <int D>
 struct GatherLane {
-  int ch;         // 16-byte chunk within a row
-  int row_lo;     // lane / CHUNKS: row offset inside the copy's row group
+  static constexpr int NRB = 4 / GatherCfg<D>::ROWS_PER_COPY;   // row blocks per slot (2 or 1)
+  int row_lo;                  // lane / CHUNKS
+  uint32_t src_off;            // row_lo * ROW_BYTES + ch * 16
+  uint32_t dst_off[2][NRB];    // row * ROW_BYTES + ((ch ^ ((sig&1)*4 + row)) << 4)
 };
 
 template <int D>
 __device__ __forceinline__ GatherLane<D> gather_lane(int lane) {
+  using C = GatherCfg<D>;
   GatherLane<D> g;
-  g.ch = lane % GatherCfg<D>::CHUNKS;
-  g.row_lo = lane / GatherCfg<D>::CHUNKS;
+  const int ch = lane % C::CHUNKS;
+  g.row_lo = lane / C::CHUNKS;
+  g.src_off = (uint32_t)(g.row_lo * C::ROW_BYTES + ch * 16);
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int rb = 0; rb < GatherLane<D>::NRB; ++rb) {
+      const int row = rb * C::ROWS_PER_COPY + g.row_lo;
+      g.dst_off[a][rb] = (uint32_t)(row * C::ROW_BYTES + ((ch ^ (a * 4 + row)) << 4));
+    }
   return g;
 }
 
@@ -79,21 +96,22 @@ __device__ __forceinline__ void gather_step16(uint32_t stage, const __nv_bfloat1
                                               const __nv_bfloat16* __restrict__ V, const int (&pools)[4],
                                               const GatherLane<D>& gl, int64_t t, int k, int grp) {
   using C = GatherCfg<D>;
+  constexpr int NRB = GatherLane<D>::NRB;
+  constexpr int POOL_BYTES = 4 * C::ROW_BYTES;
 #pragma unroll
-  for (int i = 0; i < C::COPIES; ++i) {
-    // copy i covers rows [row0, row0 + ROWS_PER_COPY) of one (slot, tensor)
-    constexpr int per_slot = 2 * 4 / C::ROWS_PER_COPY;       // copies per slot (both tensors)
-    const int sig = i / per_slot;
-    const int ten = (i % per_slot) / (per_slot / 2);
-    const int row = (i % (per_slot / 2)) * C::ROWS_PER_COPY + gl.row_lo;
+  for (int sig = 0; sig < 4; ++sig) {
     const int p = pools[sig];
     const int nrows = slot_rows(p, grp * 4 + sig, k, t);
-    const bool valid = row < nrows;
-    const __nv_bfloat16* base = ten ? V : K;
-    const __nv_bfloat16* src = base + (valid ? ((int64_t)(4 * p + row) * D + gl.ch * 8) : 0);
-    const int key = sig * 4 + row;
-    const uint32_t dst = stage + ten * C::TILE_BYTES + key * C::ROW_BYTES + ((gl.ch ^ (key & 7)) << 4);
-    cp_async16(dst, src, valid ? 16u : 0u);
+    const int64_t pool_off = (int64_t)(p < 0 ? 0 : p) * POOL_BYTES + gl.src_off;   // a valid address even if unused
+    const char* srcK = reinterpret_cast<const char*>(K) + pool_off;
+    const char* srcV = reinterpret_cast<const char*>(V) + pool_off;
+#pragma unroll
+    for (int rb = 0; rb < NRB; ++rb) {
+      const uint32_t bytes = rb * C::ROWS_PER_COPY + gl.row_lo < nrows ? 16u : 0u;
+      const uint32_t dst = stage + sig * POOL_BYTES + gl.dst_off[sig & 1][rb];
+      cp_async16(dst, srcK + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
+      cp_async16(dst + C::TILE_BYTES, srcV + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
+    }
   }
 }
 
