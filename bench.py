@@ -130,6 +130,20 @@ def algorithmic(wl):
     }
 
 
+# ------------------------------------------------------------ replicas
+def aggregate_replicas(local_ms: float, local_tokens: int, world: int, device=None):
+    """Whole-job throughput of N independent replicas: every rank's tokens
+    divided by the slowest rank's time.  Returns (tokens/s, max ms, tokens)."""
+    if world > 1:
+        t = torch.tensor([local_ms, float(local_tokens)], dtype=torch.float64, device=device)
+        mx = t[:1].clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        tot = t[1:].clone()
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.SUM)
+        local_ms, local_tokens = float(mx.item()), int(tot.item())
+    return local_tokens / (local_ms / 1e3), local_ms, local_tokens
+
+
 # -------------------------------------------------------------------- ours
 def run_ours(args, rank, world):
     import long_context_sparse_dsa_gb300 as dsa
@@ -154,12 +168,13 @@ def run_ours(args, rank, world):
     dq = torch.empty((wl.L, wl.Hq, wl.d), device=dev) if with_bwd else None
     dk = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
     dv = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
+    bws = dsa.alloc_backward_workspace(dims, dev) if with_bwd else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
     stream = torch.cuda.current_stream(dev)
     scores = bufs.ws.view(torch.float32)
     C = wl.q_chunk
     chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
-    launches_per_step = 1 + 2 * len(chunks) + 1 + (1 if with_bwd else 0)
+    launches_per_step = 1 + 2 * len(chunks) + 1 + (2 if with_bwd else 0)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -188,7 +203,7 @@ def run_ours(args, rank, world):
             marks[-1][1].record(stream)
         if with_bwd:
             dsa.sparse_attn_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq,
-                                dk, dv, None, 0, stream)
+                                dk, dv, bws, None, stream)
             if timers is not None:
                 marks.append(("attn_bwd", timers.pop()))
                 marks[-1][1].record(stream)
@@ -219,13 +234,7 @@ def run_ours(args, rank, world):
             torch.distributed.barrier()
     dsa.check_device_error(stream)
 
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = wl.L * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value, total_ms, tokens = aggregate_replicas(sum(step_ms), wl.L * args.steps, world, dev)
 
     # kernel totals per step (sum over chunk launches) and per-launch means
     steps = args.steps
@@ -239,7 +248,7 @@ def run_ours(args, rank, world):
                     **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))} for nm in k_ms}
 
     # end-to-end through the C ABI with host buffers: H2D of the inputs, the layer, D2H of the results
-    e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_bwd, world, dev)
+    e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev)
     clocks = clk.summary()
     return {
         "metric": METRIC if args.workload == "bf16_128k_needle" else f"DSA-layer tokens/s ({wl.passes}) {wl.name}",
@@ -278,7 +287,7 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks):
             "traffic": None, "peak_source": f"{peak_kind} HBM copy"}
 
 
-def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_bwd, world, dev):
+def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev):
     names = list(d_in.keys())
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
@@ -293,7 +302,7 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_b
                       bufs.idx, bufs.kpool, bufs.ws, stream=stream)
         if with_bwd:
             dsa.layer_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq, dk, dv,
-                          stream=stream)
+                          bws, stream=stream)
         for src, dst in zip(outs, pinned_out):
             dst.copy_(src, non_blocking=True)
 
@@ -305,12 +314,8 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, stream, args, with_b
         one()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(wl.L * steps * world / (ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    value, ms, _ = aggregate_replicas(e0.elapsed_time(e1), wl.L * steps, world, dev)
+    return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 

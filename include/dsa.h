@@ -114,8 +114,14 @@ dsa_status dsa_validate_dims(const dsa_dims *dims, int32_t with_backward);
 
 /* Bytes of device workspace dsa_layer_fwd needs: the fp32 score block of one
  * query chunk, q_chunk * (L/4) * 4 bytes, rounded up to 256.  Returns 0 if
- * dims are invalid.  dsa_layer_bwd and dsa_sparse_attn_bwd need none. */
+ * dims are invalid. */
 size_t dsa_workspace_bytes(const dsa_dims *dims);
+
+/* Bytes of device workspace dsa_sparse_attn_bwd / dsa_layer_bwd need: one
+ * fp32 value per (query, head), L * Hq * 4 bytes, rounded up to 256 (it holds
+ * D[t,h] = dO[t,h] . O[t,h] between the backward's two kernels).  Returns 0
+ * if dims are invalid for a backward. */
+size_t dsa_bwd_workspace_bytes(const dsa_dims *dims);
 
 /* Pool keys.  Page "SkyRL extends GLM-5.3-Flash ...", section "Model and
  * bottleneck" (one pool per 4 tokens).
@@ -161,8 +167,11 @@ dsa_status dsa_sparse_attn_fwd(const dsa_dims *dims, const void *q, const void *
  *   dq [L, Hq, d] fp32 (overwritten), dk, dv [L, d] fp32 (zeroed on the
  *   stream, then accumulated with fp32 atomics).
  * o and lse must be the forward's outputs for the same q, k, v, idx.  The
- * selection is piecewise constant: no gradient reaches the indexer inputs.
- * ws/ws_bytes are accepted for ABI stability and may be NULL/0. */
+ * kernels form D = dO . O as sum_j P_j dP_j from the exact P and dP (a first
+ * kernel, into ws), so the bf16 rounding of o does not enter the gradients;
+ * o itself is validated but not read.  The selection is piecewise constant:
+ * no gradient reaches the indexer inputs.
+ *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory (scratch) */
 dsa_status dsa_sparse_attn_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
                                const int32_t *idx, const void *o, const float *lse, const void *dout,
                                float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
@@ -178,7 +187,8 @@ dsa_status dsa_layer_fwd(const dsa_dims *dims, const void *q, const void *k, con
                          void *ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* Whole backward: dsa_sparse_attn_bwd with the idx and lse the forward
- * saved (the indexer is not recomputed and gets no gradient). */
+ * saved (the indexer is not recomputed and gets no gradient).
+ *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory */
 dsa_status dsa_layer_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
                          const int32_t *idx, const void *o, const float *lse, const void *dout,
                          float *dq, float *dk, float *dv, void *ws, size_t ws_bytes, dsa_stream_t stream);

@@ -8,8 +8,8 @@ or no GPU is present, calls raise.
 
 Entry points (same names as the C ABI, without the ``dsa_`` prefix):
 pool_keys, indexer_score, topk, sparse_attn_fwd, sparse_attn_bwd,
-layer_fwd, layer_bwd, check_device_error, workspace_bytes, validate_dims,
-layer_fwd_noalloc.
+layer_fwd, layer_bwd, check_device_error, workspace_bytes, bwd_workspace_bytes,
+validate_dims, layer_fwd_noalloc.
 """
 from __future__ import annotations
 
@@ -62,6 +62,7 @@ def _load():
             "dsa_last_error_message": ([], ctypes.c_char_p),
             "dsa_validate_dims": ([D, i32], ctypes.c_int),
             "dsa_workspace_bytes": ([D], ctypes.c_size_t),
+            "dsa_bwd_workspace_bytes": ([D], ctypes.c_size_t),
             "dsa_pool_keys": ([D, P, P, P], ctypes.c_int),
             "dsa_indexer_score": ([D, P, P, P, i64, i64, P, P], ctypes.c_int),
             "dsa_topk": ([D, P, i64, i64, P, P], ctypes.c_int),
@@ -131,6 +132,10 @@ def workspace_bytes(dims: Dims) -> int:
     return int(_load().dsa_workspace_bytes(ctypes.byref(dims)))
 
 
+def bwd_workspace_bytes(dims: Dims) -> int:
+    return int(_load().dsa_bwd_workspace_bytes(ctypes.byref(dims)))
+
+
 def pool_keys(dims, k_idx, kpool, stream=None):
     _check(_load().dsa_pool_keys(ctypes.byref(dims), _ptr(k_idx), _ptr(kpool), _stream(stream)), "dsa_pool_keys")
 
@@ -150,7 +155,9 @@ def sparse_attn_fwd(dims, q, k, v, idx, o, lse, stream=None):
                                        _stream(stream)), "dsa_sparse_attn_fwd")
 
 
-def sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=0, stream=None):
+def sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_sparse_attn_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
                                        _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                        _stream(stream)), "dsa_sparse_attn_bwd")
@@ -171,7 +178,9 @@ def layer_fwd_noalloc(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, stream
            "dsa_layer_fwd_noalloc")
 
 
-def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=0, stream=None):
+def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_layer_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                  _stream(stream)), "dsa_layer_bwd")
@@ -197,6 +206,14 @@ class LayerBuffers:
     idx: object
     kpool: object
     ws: object
+
+
+def alloc_backward_workspace(dims: Dims, device="cuda"):
+    import torch
+    n = bwd_workspace_bytes(dims)
+    if n == 0:
+        _check(validate_dims(dims, True), "dsa_bwd_workspace_bytes")
+    return torch.empty((n,), dtype=torch.uint8, device=device)
 
 
 def alloc_forward_buffers(dims: Dims, device="cuda") -> LayerBuffers:

@@ -128,13 +128,18 @@ dsa_status do_fwd(const dsa_dims* d, const void* q, const void* k, const void* v
   return cuda_status(e, "sparse_attn_fwd launch");
 }
 
-dsa_status do_bwd(const dsa_dims* d, const void* q, const void* k, const void* v, const int32_t* idx, const void* o,
-                  const float* lse, const void* dout, float* dq, float* dk, float* dv, cudaStream_t s) {
+size_t bwd_ws_bytes(const dsa_dims* d) {
+  const size_t bytes = (size_t)d->L * (size_t)d->Hq * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+dsa_status do_bwd(const dsa_dims* d, const void* q, const void* k, const void* v, const int32_t* idx,
+                  const float* lse, const void* dout, float* dq, float* dk, float* dv, float* dbuf, cudaStream_t s) {
   const size_t kv_bytes = (size_t)d->L * d->d * sizeof(float);
   cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, s);
   if (e != cudaSuccess) return cuda_status(e, "zeroing dk/dv");
-  e = dsa::launch_attn_bwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, dout, dq, dk, dv, s);
+  e = dsa::launch_attn_bwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, lse, dout, dbuf, dq, dk, dv, s);
   return cuda_status(e, "sparse_attn_bwd launch");
 }
 
@@ -223,11 +228,14 @@ dsa_status dsa_sparse_attn_fwd(const dsa_dims* dims, const void* q, const void* 
   return do_fwd(dims, q, k, v, idx, o, lse, (cudaStream_t)stream);
 }
 
+size_t dsa_bwd_workspace_bytes(const dsa_dims* dims) {
+  if (check_dims(dims, true) != DSA_OK) return 0;
+  return bwd_ws_bytes(dims);
+}
+
 dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* k, const void* v,
                                const int32_t* idx, const void* o, const float* lse, const void* dout, float* dq,
                                float* dk, float* dv, void* ws, size_t ws_bytes, dsa_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   g_msg[0] = 0;
   dsa_status st = check_dims(dims, true);
   if (st) return st;
@@ -242,7 +250,11 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* 
   REQUIRE_PTR(dk);
   REQUIRE_PTR(dv);
   if (dk == dv) return fail(DSA_ERR_INVALID_ARG, "dk and dv must not alias");
-  return do_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, (cudaStream_t)stream);
+  const size_t need = bwd_ws_bytes(dims);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "backward workspace of %zu bytes given, %zu needed", ws_bytes, need);
+  if (!aligned16(ws)) return fail(DSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  return do_bwd(dims, q, k, v, idx, lse, dout, dq, dk, dv, static_cast<float*>(ws), (cudaStream_t)stream);
 }
 
 dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, const void* v, const void* q_idx,

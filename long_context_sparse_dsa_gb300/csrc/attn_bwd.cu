@@ -11,8 +11,11 @@
 //   dK[j] += scale sum_h dS Q[t,h],  dV[j] += sum_h P dO[t,h].
 // The selection is piecewise constant, so q_I, k_I and w get no gradient.
 //
-// One warp per (query, 16-head group), the same 16-key gather pipeline as
-// the forward.  dQ stays in registers for the whole query.  Per 16-key step
+// Two kernels, one warp per (query, 16-head group) each, with the same 16-key
+// gather pipeline as the forward.  The first forms D[t,h] = sum_j P_j dP_j
+// into a [L, Hq] fp32 workspace; the second does everything else, so the
+// atomic traffic of the second is not interleaved with a pass that has none.
+// dQ stays in registers for the whole query.  Per 16-key step
 // the warp computes the 16x16 S and dP tiles with m16n8k16 MMAs (heads on M),
 // then the 16-key x d tiles of dK and dV with the keys on M: the transposed
 // P and dS operands are built in registers with movmatrix, and Q / dO come
@@ -27,7 +30,9 @@
 
 namespace dsa {
 
-template <int D>
+// PASS 1 forms D[t,h] = sum_j P_j dP_j into a [L, Hq] fp32 buffer; PASS 2
+// forms dS and the gradients.  PASS 2 also keeps fp16 copies of Q and dO.
+template <int D, int PASS>
 struct BwdCfg {
   static constexpr int ROW_BYTES = GatherCfg<D>::ROW_BYTES;
   static constexpr int CHUNKS = GatherCfg<D>::CHUNKS;
@@ -35,7 +40,7 @@ struct BwdCfg {
   static constexpr int STAGE_BYTES = GatherCfg<D>::STAGE_BYTES;
   static constexpr int NST = 2;
   static constexpr int WARPS = 4;
-  static constexpr int WARP_BYTES = NST * STAGE_BYTES + 2 * TILE_BYTES;  // stages + Q + dO copies
+  static constexpr int WARP_BYTES = NST * STAGE_BYTES + (PASS == 2 ? 2 * TILE_BYTES : 0);
   static constexpr int SMEM = WARPS * WARP_BYTES;
 };
 
@@ -49,13 +54,13 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <int D>
+template <int D, int PASS>
 __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-    const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ O, const float* __restrict__ LSE,
-    const __nv_bfloat16* __restrict__ dO, float* __restrict__ dQ, float* __restrict__ dK, float* __restrict__ dV,
-    int64_t L, int Hq, int k, float scale, float scale_log2) {
-  using C = BwdCfg<D>;
+    const int32_t* __restrict__ idx, const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ dO,
+    float* __restrict__ Dbuf, float* __restrict__ dQ, float* __restrict__ dK, float* __restrict__ dV, int64_t L,
+    int Hq, int k, float scale, float scale_log2) {
+  using C = BwdCfg<D, PASS>;
   extern __shared__ __align__(128) unsigned char bwd_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HG = Hq / 16;
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 
   // Per-warp swizzled fp16 copies of Q and dO (16 heads x D), 16-byte chunks;
   // the B operands of the dK and dV products.
-  {
+  if (PASS == 2) {
     const uint4* q4 = reinterpret_cast<const uint4*>(Q + row0 * D);
     const uint4* d4 = reinterpret_cast<const uint4*>(dO + row0 * D);
     unsigned char* qsp = bwd_smem + (qs - smem_u32(bwd_smem));
@@ -115,27 +120,31 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) dq[n][0] = dq[n][1] = dq[n][2] = dq[n][3] = 0.f;
 
-  // Two passes over the key groups through one gather pipeline: pass 1 forms
-  // D[h] = sum_j P_j dP_j (equal to dO . O, but from the exact P and dP rather
-  // than the bf16-rounded O), pass 2 forms dS and the gradients.
+  // One pass over the key groups.  PASS 1 accumulates D[h] = sum_j P_j dP_j
+  // (equal to dO . O, but from the exact P and dP rather than the
+  // bf16-rounded O); PASS 2 reads it back and forms dS and the gradients.
   static_assert(C::NST == 2, "the pool ring below is written for two stages");
   const GatherLane<D> gl = gather_lane<D>(lane);
-  const int nsteps = 2 * ngroups;
+  const int nsteps = ngroups;
   int pc[4];
   step_pools(irow, k, 0, t, lane, pc);
   gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
   cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
+  if (PASS == 2) {
+    Dg = __ldg(Dbuf + row0 + g);
+    Dg8 = __ldg(Dbuf + row0 + g + 8);
+  }
 
   for (int step = 0; step < nsteps; ++step) {
-    const bool pass1 = step < ngroups;
-    const int grp = pass1 ? step : step - ngroups;
+    constexpr bool pass1 = PASS == 1;
+    const int grp = step;
     const int stage = step & 1;
     int pf[4] = {-1, -1, -1, -1};
     {
       const int nx = step + 1;
       if (nx < nsteps) {
-        const int grp_n = nx < ngroups ? nx : nx - ngroups;
+        const int grp_n = nx;
         step_pools(irow, k, grp_n, t, lane, pf);
         gather_step16<D>(wbase + (nx & 1) * C::STAGE_BYTES, K, V, pf, gl, t, k, grp_n);
       }
@@ -214,12 +223,6 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
           Dg = fmaf(ex2_approx(s[nt][1] * scale_log2 - lse_g), dp[nt][1], Dg);
           Dg8 = fmaf(ex2_approx(s[nt][3] * scale_log2 - lse_g8), dp[nt][3], Dg8);
         }
-      }
-      if (step == ngroups - 1) {
-        Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
-        Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);
-        Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 1);
-        Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 2);
       }
       __syncwarp();
 #pragma unroll
@@ -300,6 +303,17 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
   }
   cp_async_wait<0>();
+  if (PASS == 1) {
+    Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
+    Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);
+    Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 1);
+    Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 2);
+    if (qi == 0) {
+      Dbuf[row0 + g] = Dg;
+      Dbuf[row0 + g + 8] = Dg8;
+    }
+    return;
+  }
 
   float* q0 = dQ + (row0 + g) * D + 2 * qi;
   float* q8 = q0 + 8 * D;
@@ -310,33 +324,41 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   }
 }
 
-cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
-                                 const void* v, const int32_t* idx, const void* o, const float* lse,
-                                 const void* dout, float* dq, float* dk, float* dv, cudaStream_t s) {
+template <int D, int PASS>
+static cudaError_t launch_pass(int64_t L, int Hq, int k, float scale, const __nv_bfloat16* q, const __nv_bfloat16* kk,
+                               const __nv_bfloat16* v, const int32_t* idx, const float* lse,
+                               const __nv_bfloat16* dout, float* dbuf, float* dq, float* dk, float* dv,
+                               cudaStream_t s) {
+  using C = BwdCfg<D, PASS>;
   const float scale_log2 = scale * 1.4426950408889634f;
   const int64_t items = L * (Hq / 16);
-  const int64_t blocks = (items + 3) / 4;
+  const int64_t blocks = (items + C::WARPS - 1) / C::WARPS;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<D, PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM);
+  if (e != cudaSuccess) return e;
+  attn_bwd_bf16_kernel<D, PASS><<<(unsigned)blocks, 32 * C::WARPS, C::SMEM, s>>>(
+      q, kk, v, idx, lse, dout, dbuf, dq, dk, dv, L, Hq, k, scale, scale_log2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                 const void* v, const int32_t* idx, const float* lse, const void* dout,
+                                 float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s) {
   auto qp = static_cast<const __nv_bfloat16*>(q);
   auto kp = static_cast<const __nv_bfloat16*>(kk);
   auto vp = static_cast<const __nv_bfloat16*>(v);
-  auto op = static_cast<const __nv_bfloat16*>(o);
   auto gp = static_cast<const __nv_bfloat16*>(dout);
+  cudaError_t e;
   if (d == 128) {
-    constexpr int smem = BwdCfg<128>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_bwd_bf16_kernel<128><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, gp, dq, dk, dv, L, Hq,
-                                                                  k, scale, scale_log2);
+    e = launch_pass<128, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
+    if (e == cudaSuccess) e = launch_pass<128, 2>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
   } else if (d == 64) {
-    constexpr int smem = BwdCfg<64>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_bwd_bf16_kernel<64><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, gp, dq, dk, dv, L, Hq,
-                                                                 k, scale, scale_log2);
+    e = launch_pass<64, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
+    if (e == cudaSuccess) e = launch_pass<64, 2>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
   } else {
-    return cudaErrorNotSupported;
+    e = cudaErrorNotSupported;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dsa

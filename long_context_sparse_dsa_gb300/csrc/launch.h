@@ -31,10 +31,11 @@ cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, c
 cudaError_t launch_attn_fwd_f32(int64_t L, int Hq, int d, int k, float scale, const float* q, const float* kk,
                                 const float* v, const int32_t* idx, float* o, float* lse, cudaStream_t s);
 
-// Sparse attention backward (bf16): dq overwritten; dk, dv must be zeroed by the caller.
+// Sparse attention backward (bf16): dq overwritten; dk, dv must be zeroed by the
+// caller; dbuf is an [L, Hq] fp32 workspace (D per query row).
 cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
-                                 const void* v, const int32_t* idx, const void* o, const float* lse,
-                                 const void* dout, float* dq, float* dk, float* dv, cudaStream_t s);
+                                 const void* v, const int32_t* idx, const float* lse, const void* dout,
+                                 float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s);
 
 int device_sm_count();
 

@@ -59,6 +59,11 @@ def test_fp32_backward_is_rejected_not_faked(lib):
     assert dsa.validate_dims(_dims(Hq=8, dtype="fp32"), with_backward=True) == dsa.DSA_ERR_UNSUPPORTED
 
 
+def test_bwd_workspace_bytes(lib):
+    assert dsa.bwd_workspace_bytes(_dims(L=131072)) == 131072 * 16 * 4
+    assert dsa.bwd_workspace_bytes(_dims(Hq=8, dtype="fp32")) == 0     # no fp32 backward
+
+
 def test_workspace_bytes(lib):
     assert dsa.workspace_bytes(_dims(L=131072, q_chunk=8192)) == 8192 * 32768 * 4
     assert dsa.workspace_bytes(_dims(L=4096, q_chunk=100)) == (100 * 1024 * 4 + 255) // 256 * 256
@@ -82,6 +87,10 @@ def test_null_and_misaligned_pointers_fail_before_launch(lib):
     # aliased gradient outputs
     assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, None, 0, None) == \
         dsa.DSA_ERR_INVALID_ARG
+    # the backward needs its D workspace
+    q = ctypes.c_void_p(512)
+    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, q, None, 0, None) == \
+        dsa.DSA_ERR_WORKSPACE
     assert lib.dsa_selftest_bounded_wait(0, None) == dsa.DSA_ERR_INVALID_ARG
 
 

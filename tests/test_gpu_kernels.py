@@ -201,7 +201,8 @@ def test_attn_bwd_matches_oracle(Hq, d, k):
     dq = torch.empty((L, Hq, d), device=DEV)
     dk = torch.full((L, d), 5.0, device=DEV)     # must be overwritten, not accumulated into
     dv = torch.full((L, d), 5.0, device=DEV)
-    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv)
+    ws = dsa.alloc_backward_workspace(dims, DEV)
+    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws)
     dsa.check_device_error()
     dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
     errs = {name: float(np.abs(got.cpu().numpy() - ref).max())

@@ -47,7 +47,8 @@ def _run_layer(wl, host, with_bwd, q_chunk=None):
         dq = torch.empty((wl.L, wl.Hq, wl.d), device=DEV)
         dk = torch.empty((wl.L, wl.d), device=DEV)
         dv = torch.empty((wl.L, wl.d), device=DEV)
-        dsa.layer_bwd(dims, dev["Q"], dev["K"], dev["V"], bufs.idx, bufs.o, bufs.lse, dev["dO"], dq, dk, dv)
+        ws = dsa.alloc_backward_workspace(dims, DEV)
+        dsa.layer_bwd(dims, dev["Q"], dev["K"], dev["V"], bufs.idx, bufs.o, bufs.lse, dev["dO"], dq, dk, dv, ws)
         out.update(dq=dq, dk=dk, dv=dv)
     dsa.check_device_error()
     return out
