@@ -21,9 +21,11 @@
 // P and dS operands are built in registers with movmatrix, and Q / dO come
 // from a per-warp swizzled shared copy.  The dK/dV products run in fp16
 // (P, scale*dS, Q, dO converted; 10-bit mantissa instead of bf16's 7) because
-// those sums collect contributions from every query that selected a key.  Each finished dK/dV fragment goes to
-// global memory with fp32 vector reductions (red.global.add.v2.f32), so the
-// summation order across queries is not fixed.
+// those sums collect contributions from every query that selected a key.
+// Each finished 16-key dK/dV tile is staged in shared memory and added to
+// global memory one key row per warp instruction (red.global.add.v4.f32 over
+// a contiguous 512-byte row), which the L2 absorbs about 1.6x faster than
+// fragment-shaped reductions; the summation order across queries is not fixed.
 #include "common.cuh"
 #include "gather.cuh"
 #include "launch.h"
@@ -160,15 +162,6 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 #pragma unroll
       for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
     }
-    // tokens of the dK/dV fragment rows this lane adds into: keys g and g+8
-    int64_t tok_lo, tok_hi;
-    {
-      const int slo = g >> 2, row = g & 3;
-      const int p_lo = slo ? pc[1] : pc[0];
-      const int p_hi = slo ? pc[3] : pc[2];
-      tok_lo = row < slot_rows(p_lo, grp * 4 + slo, k, t) ? 4 * (int64_t)p_lo + row : -1;
-      tok_hi = row < slot_rows(p_hi, grp * 4 + 2 + slo, k, t) ? 4 * (int64_t)p_hi + row : -1;
-    }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
     const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
@@ -264,38 +257,53 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const uint32_t pt2 = movmatrix_t(pp[0][1]), pt3 = movmatrix_t(pp[1][1]);
     const uint32_t dt0 = movmatrix_t(dh[0][0]), dt1 = movmatrix_t(dh[1][0]);
     const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
+    // The step's K/V stage is free now (S, dP and dQ are done).  Each 16-key
+    // fp32 tile (dV, then dK) is written into it, 16-byte chunk c of row r at
+    // position c ^ (r & 7) (conflict-free for both the fragment writes and the
+    // row reads), and then added to global memory one key row at a time: the
+    // whole warp covers a row with one contiguous vector reduction.
+    __syncwarp();
     {
+      constexpr int RCH = D / 4;              // 16-byte chunks per fp32 row
+      constexpr int RBYTES = D * 4;
+      constexpr int ROWS_PER_RED = 32 / RCH;  // rows covered by one warp instruction
       const int mtx = lane >> 3, r = lane & 7;
       const int hrow = (mtx & 1) * 8 + r;
-      float* dv_lo = tok_lo >= 0 ? dV + tok_lo * D + 2 * qi : nullptr;
-      float* dv_hi = tok_hi >= 0 ? dV + tok_hi * D + 2 * qi : nullptr;
-      float* dk_lo = tok_lo >= 0 ? dK + tok_lo * D + 2 * qi : nullptr;
-      float* dk_hi = tok_hi >= 0 ? dK + tok_hi * D + 2 * qi : nullptr;
+      const uint32_t tile = ks_base;
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        const int ch = 2 * j + (mtx >> 1);
-        const uint32_t off = hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        float cv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        ldsm_x4_t(dos + off, b0, b1, b2, b3);
-        mma_f16_16816(cv[0], pt0, pt1, pt2, pt3, b0, b1);
-        mma_f16_16816(cv[1], pt0, pt1, pt2, pt3, b2, b3);
-        float ck[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        ldsm_x4_t(qs + off, b0, b1, b2, b3);
-        mma_f16_16816(ck[0], dt0, dt1, dt2, dt3, b0, b1);
-        mma_f16_16816(ck[1], dt0, dt1, dt2, dt3, b2, b3);
+      for (int which = 0; which < 2; ++which) {   // 0: dV = P^T dO, 1: dK = (scale dS)^T Q
+        const uint32_t bsrc = which ? qs : dos;
+        const uint32_t a0 = which ? dt0 : pt0, a1 = which ? dt1 : pt1;
+        const uint32_t a2 = which ? dt2 : pt2, a3 = which ? dt3 : pt3;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col = (2 * j + h) * 8;
-          if (dv_lo) {
-            red_add_v2(dv_lo + col, cv[h][0], cv[h][1]);
-            red_add_v2(dk_lo + col, ck[h][0], ck[h][1]);
-          }
-          if (dv_hi) {
-            red_add_v2(dv_hi + col, cv[h][2], cv[h][3]);
-            red_add_v2(dk_hi + col, ck[h][2], ck[h][3]);
+        for (int j = 0; j < D / 16; ++j) {
+          const int ch = 2 * j + (mtx >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(bsrc + hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4), b0, b1, b2, b3);
+          float c2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          mma_f16_16816(c2[0], a0, a1, a2, a3, b0, b1);
+          mma_f16_16816(c2[1], a0, a1, a2, a3, b2, b3);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = (2 * j + h) * 2 + (qi >> 1);          // fp32 chunk of columns (2j+h)*8 + 2qi
+            const uint32_t off = (uint32_t)(((c ^ (g & 7)) << 4) + (qi & 1) * 8);
+            st_shared_v2(tile + g * RBYTES + off, c2[h][0], c2[h][1]);
+            st_shared_v2(tile + (g + 8) * RBYTES + off, c2[h][2], c2[h][3]);
           }
         }
+        __syncwarp();
+        float* gdst = which ? dK : dV;
+#pragma unroll
+        for (int kk0 = 0; kk0 < 16; kk0 += ROWS_PER_RED) {
+          const int kk = kk0 + lane / RCH;                    // the row this lane adds
+          const int lc = lane % RCH;
+          const int sig = kk >> 2, row = kk & 3;
+          const int pool = sig == 0 ? pc[0] : sig == 1 ? pc[1] : sig == 2 ? pc[2] : pc[3];
+          const bool ok = row < slot_rows(pool, grp * 4 + sig, k, t);
+          const float4 v = ld_shared_v4(tile + kk * RBYTES + ((lc ^ (kk & 7)) << 4));
+          if (ok) red_add_v4(gdst + (4 * (int64_t)pool + row) * D + lc * 4, v);
+        }
+        __syncwarp();
       }
     }
     __syncwarp();
