@@ -137,8 +137,11 @@ dsa_status dsa_pool_keys(const dsa_dims *dims, const void *k_idx, void *kpool, d
  *   q_idx   [L, Hi, di] layer dtype, indexer queries q_I
  *   kpool   [L/4, di]   layer dtype, from dsa_pool_keys
  *   w       [L, Hi]     fp32 head weights
- *   scores  [q_count, L/4] fp32, output; row r is query q_begin+r.  Only
- *           entries p < elig(q_begin+r) are written; the rest are untouched.
+ *   scores  [q_count, L/4] fp32, output; row r is query q_begin+r.  The
+ *           entries p < elig(q_begin+r) hold the scores.  Entries past that
+ *           prefix are unspecified: those inside the last 128-pool tile a
+ *           32-query block visits may be overwritten, later ones are not
+ *           touched.
  * Requires 0 <= q_begin, q_count >= 1, q_begin+q_count <= L. */
 dsa_status dsa_indexer_score(const dsa_dims *dims, const void *q_idx, const void *kpool, const float *w,
                              int64_t q_begin, int64_t q_count, float *scores, dsa_stream_t stream);

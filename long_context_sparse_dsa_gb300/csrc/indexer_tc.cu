@@ -23,8 +23,11 @@
 //     TMEM and issues the MMAs from one thread; warps 2..9 run the epilogue
 //     (two warps per TMEM lane quarter, each taking 16 of the 32 queries).
 //   * Work unit = (32-query block, up to kSeg pool tiles).  Pool tiles wholly
-//     in the future of every query of the block are never visited; the
-//     diagonal tile is masked at the store.  Units are handed out round-robin
+//     in the future of every query of the block are never visited.  Each
+//     epilogue warp stages its 16 queries x 32 pools of a tile in shared
+//     memory and writes them with one TMA store (entries past a query's
+//     causal prefix inside the diagonal tile are written too; nothing reads
+//     them).  Units are handed out round-robin
 //     to the persistent CTAs, later (longer) query blocks first.
 //   * Every mbarrier wait is bounded; on expiry the CTA records a timeout,
 //     unwinds, and still frees its TMEM.
@@ -55,8 +58,12 @@ struct IdxCfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NSA * A_BYTES;
   static constexpr int OFF_W = OFF_B + 2 * B_BYTES;
-  static constexpr int OFF_BAR = OFF_W + 8 * 16 * HI * 4;  // private w slice per epilogue warp
+  static constexpr int OFF_STG = OFF_W + 8 * 16 * HI * 4;  // private w slice per epilogue warp
+  static constexpr int NSTG = DI == 64 ? 2 : 1;            // score staging buffers per epilogue warp
+  static constexpr int STG_BYTES = 16 * 32 * 4;            // 16 queries x 32 pools fp32
+  static constexpr int OFF_BAR = OFF_STG + 8 * NSTG * STG_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 struct UnitIter {
@@ -89,8 +96,8 @@ struct UnitIter {
 template <int HI, int DI>
 __global__ void __launch_bounds__(320, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
-                      const float* __restrict__ w, float* __restrict__ scores, int64_t P, int64_t q_begin,
-                      int64_t q_count) {
+                      const __grid_constant__ CUtensorMap tmap_s, const float* __restrict__ w,
+                      float* __restrict__ scores, int64_t P, int64_t q_begin, int64_t q_count, int tma_store) {
   using C = IdxCfg<HI, DI>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -130,6 +137,7 @@ __global__ void __launch_bounds__(320, 1)
     fence_mbar_init();
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_kp);
+    if (tma_store) prefetch_tmap(&tmap_s);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t acc_iter = 0;
     bool ok = true;
     float* w_mine = w_s + ew * 16 * HI;      // this warp's 16 queries x HI weights
+    uint32_t stg_iter = 0;
     while (ok && it.next<C::BN, C::BM, C::SEG>()) {
       __syncwarp();
       for (int i = lane; i < 16 * HI; i += 32) {
@@ -278,16 +287,39 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         const int64_t p = tile * C::BM + lane_base + lane;
+        if (tma_store) {
+          // stage this warp's 16 queries x 32 pools and store them with one
+          // TMA box; entries past a query's causal prefix inside the box are
+          // written too (the top-k never reads them)
+          const int sb = stg_iter % C::NSTG;
+          const uint32_t stg = smem_u32(smem + C::OFF_STG) + (ew * C::NSTG + sb) * C::STG_BYTES;
+          if (lane == 0 && stg_iter >= C::NSTG) bulk_wait_read<C::NSTG - 1>();
+          __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int64_t t = it.t0 + half * 16 + j;
-          // streaming store: the score block is read once, by the top-k
-          if (t < q_end && p < elig(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
+          for (int j = 0; j < 16; ++j)
+            asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(stg + (j * 32 + lane) * 4), "f"(acc[j]) : "memory");
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_s, stg, (int32_t)(tile * C::BM + lane_base), (int32_t)(it.t0 - q_begin + half * 16));
+            bulk_commit();
+          }
+          ++stg_iter;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int64_t t = it.t0 + half * 16 + j;
+            // streaming store: the score block is read once, by the top-k
+            if (t < q_end && p < elig(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
+          }
         }
         ++acc_iter;
       }
     }
     if (!ok) *abort_flag = 1;
+    // every score store of this warp has finished before the CTA exits
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -340,6 +372,23 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // Score tiles go out through TMA when the row pitch allows it (P*4 a
+  // multiple of 16 bytes); otherwise with plain stores.
+  CUtensorMap ts;
+  int tma_store = 0;
+  if ((P % 4) == 0) {
+    const cuuint64_t dims[2] = {(cuuint64_t)P, (cuuint64_t)q_count};
+    const cuuint64_t strides[1] = {(cuuint64_t)P * 4};
+    const cuuint32_t box[2] = {32, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scores, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    tma_store = 1;
+  } else {
+    ts = tk;  // unused
+  }
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -350,8 +399,8 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
   if (units == 0) return cudaSuccess;
   int64_t grid = device_sm_count();
   if (grid > units) grid = units;
-  indexer_tc_kernel<HI, DI><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, w, scores, P, q_begin,
-                                                                               q_count);
+  indexer_tc_kernel<HI, DI><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, ts, w, scores, P, q_begin,
+                                                                               q_count, tma_store);
   return cudaGetLastError();
 }
 
