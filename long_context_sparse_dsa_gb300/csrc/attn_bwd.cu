@@ -259,9 +259,10 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
     // The step's K/V stage is free now (S, dP and dQ are done).  Each 16-key
     // fp32 tile (dV, then dK) is written into it, 16-byte chunk c of row r at
-    // position c ^ (r & 7) (conflict-free for both the fragment writes and the
-    // row reads), and then added to global memory one key row at a time: the
-    // whole warp covers a row with one contiguous vector reduction.
+    // position c ^ 2(r & 7): a half-warp's fragment writes (rows g..g+3, two
+    // adjacent chunks each) then hit distinct bank groups, and a row read is a
+    // permutation of the row.  It is then added to global memory one key row
+    // at a time: the whole warp covers a row with one contiguous reduction.
     __syncwarp();
     {
       constexpr int RCH = D / 4;              // 16-byte chunks per fp32 row
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int c = (2 * j + h) * 2 + (qi >> 1);          // fp32 chunk of columns (2j+h)*8 + 2qi
-            const uint32_t off = (uint32_t)(((c ^ (g & 7)) << 4) + (qi & 1) * 8);
+            const uint32_t off = (uint32_t)(((c ^ (2 * (g & 7))) << 4) + (qi & 1) * 8);
             st_shared_v2(tile + g * RBYTES + off, c2[h][0], c2[h][1]);
             st_shared_v2(tile + (g + 8) * RBYTES + off, c2[h][2], c2[h][3]);
           }
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
           const int sig = kk >> 2, row = kk & 3;
           const int pool = sig == 0 ? pc[0] : sig == 1 ? pc[1] : sig == 2 ? pc[2] : pc[3];
           const bool ok = row < slot_rows(pool, grp * 4 + sig, k, t);
-          const float4 v = ld_shared_v4(tile + kk * RBYTES + ((lc ^ (kk & 7)) << 4));
+          const float4 v = ld_shared_v4(tile + kk * RBYTES + ((lc ^ (2 * (kk & 7))) << 4));
           if (ok) red_add_v4(gdst + (4 * (int64_t)pool + row) * D + lc * 4, v);
         }
         __syncwarp();
