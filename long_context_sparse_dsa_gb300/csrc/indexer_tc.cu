@@ -20,8 +20,8 @@
 //   * Warp 0 issues TMA loads (128-byte swizzle): the q_I block of a work unit
 //     (one box of 32*Hi rows per 64-wide K chunk, double-buffered) and a ring
 //     of kpool tiles.  Warp 1 allocates
-//     TMEM and issues the MMAs from one thread; warps 2..9 run the epilogue
-//     (two warps per TMEM lane quarter, each taking 16 of the 32 queries).
+//     TMEM and issues the MMAs from one thread; warps 2..17 run the epilogue
+//     (four warps per TMEM lane quarter, each taking 8 of the 32 queries).
 //   * Work unit = (32-query block, up to kSeg pool tiles).  Pool tiles wholly
 //     in the future of every query of the block are never visited.  Each
 //     epilogue warp stages its 16 queries x 32 pools of a tile in shared
@@ -54,14 +54,17 @@ struct IdxCfg {
   static constexpr int ACC_COLS = HI * BN;            // TMEM columns per accumulator
   static constexpr int TMEM_COLS = 2 * ACC_COLS;      // 256 or 512 (power of two)
   static constexpr int SEG = 16;                      // pool tiles per work unit
-  static constexpr int THREADS = 320;
+  static constexpr int EW = 4;                        // epilogue warps per TMEM lane quarter
+  static constexpr int QPW = BN / EW;                  // queries per epilogue warp
+  static constexpr int NEPI = 4 * EW;                  // epilogue warps
+  static constexpr int THREADS = 64 + 32 * NEPI;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NSA * A_BYTES;
   static constexpr int OFF_W = OFF_B + 2 * B_BYTES;
-  static constexpr int OFF_STG = OFF_W + 8 * 16 * HI * 4;  // private w slice per epilogue warp
+  static constexpr int OFF_STG = OFF_W + NEPI * QPW * HI * 4;  // private w slice per epilogue warp
   static constexpr int NSTG = DI == 64 ? 2 : 1;            // score staging buffers per epilogue warp
-  static constexpr int STG_BYTES = 16 * 32 * 4;            // 16 queries x 32 pools fp32
-  static constexpr int OFF_BAR = OFF_STG + 8 * NSTG * STG_BYTES;
+  static constexpr int STG_BYTES = QPW * 32 * 4;           // QPW queries x 32 pools fp32
+  static constexpr int OFF_BAR = OFF_STG + NEPI * NSTG * STG_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -94,7 +97,7 @@ struct UnitIter {
 };
 
 template <int HI, int DI>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
                       const __grid_constant__ CUtensorMap tmap_s, const float* __restrict__ w,
                       float* __restrict__ scores, int64_t P, int64_t q_begin, int64_t q_count, int tma_store) {
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(full_b(s), 1);
       mbar_init(empty_b(s), 1);
       mbar_init(tfull(s), 1);
-      mbar_init(tempty(s), 8);
+      mbar_init(tempty(s), C::NEPI);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -231,18 +234,19 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int ew = warp - 2;                 // 0..7
+    const int ew = warp - 2;                 // 0 .. NEPI-1
     const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int half = ew >> 2;                // which 16 of the 32 queries
+    const int qg = ew >> 2;                  // which QPW of the 32 queries
     const int lane_base = quarter * 32;
     uint32_t acc_iter = 0;
     bool ok = true;
-    float* w_mine = w_s + ew * 16 * HI;      // this warp's 16 queries x HI weights
+    float* w_mine = w_s + ew * C::QPW * HI;  // this warp's QPW queries x HI weights
     uint32_t stg_iter = 0;
+    constexpr int NLD = C::QPW * HI / 16;    // 16-column TMEM loads per tile
     while (ok && it.next<C::BN, C::BM, C::SEG>()) {
       __syncwarp();
-      for (int i = lane; i < 16 * HI; i += 32) {
-        const int64_t t = it.t0 + half * 16 + i / HI;
+      for (int i = lane; i < C::QPW * HI; i += 32) {
+        const int64_t t = it.t0 + qg * C::QPW + i / HI;
         w_mine[i] = t < q_end ? __ldg(w + t * HI + (i % HI)) : 0.f;
       }
       __syncwarp();
@@ -250,45 +254,34 @@ __global__ void __launch_bounds__(320, 1)
         const int ab = acc_iter & 1;
         if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        // this thread: pool (lane_base + lane), queries half*16 .. +15, columns
-        // (query*Hi + head); batches of 64 columns = 64/Hi queries
-        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + half * 16 * HI;
-        constexpr int NB = 16 * HI / 64;
-        constexpr int QB = 64 / HI;                // queries per batch
-        float acc[16];
+        // this thread: pool (lane_base + lane), queries qg*QPW .. +QPW-1, columns
+        // (query*Hi + head) -- all loaded before one wait
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + qg * C::QPW * HI;
+        float v[NLD][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        for (int i = 0; i < NLD; ++i) tmem_ld16(taddr + i * 16, v[i]);
+        tmem_ld_wait();
+        // the accumulator is in registers: hand it back to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(ab));
+        float acc[C::QPW];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          float v[4][16];
+        for (int j = 0; j < C::QPW; ++j) acc[j] = 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tmem_ld16(taddr + b * 64 + i * 16, v[i]);
-          tmem_ld_wait();
-          if (b == NB - 1) {
-            // the accumulator is in registers: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty(ab));
-          }
-          // weights of this batch's queries, 4 per shared-memory load (broadcast)
-          float wv[64];
+        for (int c4 = 0; c4 < NLD * 4; ++c4) {
+          const float4 q4 = reinterpret_cast<const float4*>(w_mine)[c4];   // broadcast
+          const float wq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-          for (int i4 = 0; i4 < 16; ++i4) {
-            const float4 q4 = reinterpret_cast<const float4*>(w_mine + b * 64)[i4];
-            wv[4 * i4 + 0] = q4.x;
-            wv[4 * i4 + 1] = q4.y;
-            wv[4 * i4 + 2] = q4.z;
-            wv[4 * i4 + 3] = q4.w;
-          }
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int jl = b * QB + c / HI;         // heads of one query in order 0..Hi-1
-            acc[jl] = fmaf(fmaxf(v[c / 16][c % 16], 0.f), wv[c], acc[jl]);
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;            // heads of one query in order 0..Hi-1
+            acc[c / HI] = fmaf(fmaxf(v[c / 16][c % 16], 0.f), wq[e], acc[c / HI]);
           }
         }
         const int64_t p = tile * C::BM + lane_base + lane;
         if (tma_store) {
-          // stage this warp's 16 queries x 32 pools and store them with one
+          // stage this warp's QPW queries x 32 pools and store them with one
           // TMA box; entries past a query's causal prefix inside the box are
           // written too (the top-k never reads them)
           const int sb = stg_iter % C::NSTG;
@@ -296,19 +289,20 @@ __global__ void __launch_bounds__(320, 1)
           if (lane == 0 && stg_iter >= C::NSTG) bulk_wait_read<C::NSTG - 1>();
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < C::QPW; ++j)
             asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(stg + (j * 32 + lane) * 4), "f"(acc[j]) : "memory");
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmap_s, stg, (int32_t)(tile * C::BM + lane_base), (int32_t)(it.t0 - q_begin + half * 16));
+            tma_store_2d(&tmap_s, stg, (int32_t)(tile * C::BM + lane_base),
+                         (int32_t)(it.t0 - q_begin + qg * C::QPW));
             bulk_commit();
           }
           ++stg_iter;
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int64_t t = it.t0 + half * 16 + j;
+          for (int j = 0; j < C::QPW; ++j) {
+            const int64_t t = it.t0 + qg * C::QPW + j;
             // streaming store: the score block is read once, by the top-k
             if (t < q_end && p < elig(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
           }
@@ -379,7 +373,7 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
   if ((P % 4) == 0) {
     const cuuint64_t dims[2] = {(cuuint64_t)P, (cuuint64_t)q_count};
     const cuuint64_t strides[1] = {(cuuint64_t)P * 4};
-    const cuuint32_t box[2] = {32, 16};
+    const cuuint32_t box[2] = {32, (cuuint32_t)C::QPW};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scores, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
