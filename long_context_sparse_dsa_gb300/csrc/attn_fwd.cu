@@ -12,7 +12,7 @@
 // bf16 kernel: one warp per (query, 16-head group).  A pool's 4 K rows (and
 // 4 V rows) are one contiguous 1 KB block, so the warp gathers 4 pools = 16
 // keys per step with 16-byte cp.async copies into an XOR-swizzled shared
-// tile (3-stage ring per warp, no CTA-wide barriers).  The 16 heads of one
+// tile (2-stage ring per warp, no CTA-wide barriers).  The 16 heads of one
 // query share every gathered key, which makes heads the M=16 side of
 // m16n8k16 bf16 MMAs: S = Q K^T and O += P V, fp32 accumulation, online
 // softmax in registers.  The kernel is bound by the L2->SM gather bandwidth
@@ -23,9 +23,9 @@
 
 namespace dsa {
 
-template <int D>
+template <int D, int NST_ = 3>
 struct FwdCfg {
-  static constexpr int NST = 3;                                  // gather stages per warp
+  static constexpr int NST = NST_;                               // gather stages per warp (2 or 3)
   static constexpr int WARPS = 4;
   static constexpr int ROW_BYTES = GatherCfg<D>::ROW_BYTES;
   static constexpr int TILE_BYTES = GatherCfg<D>::TILE_BYTES;
@@ -33,15 +33,15 @@ struct FwdCfg {
   static constexpr int SMEM = WARPS * NST * STAGE_BYTES;
 };
 
-template <int D>
-__global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
+template <int D, int NST, int MINB>
+__global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
                                                             const __nv_bfloat16* __restrict__ K,
                                                             const __nv_bfloat16* __restrict__ V,
                                                             const int32_t* __restrict__ idx,
                                                             __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
                                                             int64_t L, int Hq, int k, float scale_log2) {
-  using C = FwdCfg<D>;
-  static_assert(C::NST == 3, "the pool ring below is written for three stages");
+  using C = FwdCfg<D, NST>;
+  static_assert(NST == 2 || NST == 3, "the pool ring below is written for two or three stages");
   extern __shared__ __align__(128) unsigned char fwd_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HG = Hq / 16;
@@ -75,25 +75,27 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
   for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-  // pools of the current step and the next one (steps grp+1, grp+2 are in flight)
-  int pc[4], pn[4];
+  // pools of the current step (pc) and, with three stages, of the next (pn)
+  int pc[4], pn[4] = {-1, -1, -1, -1};
   step_pools(irow, k, 0, t, lane, pc);
   gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
   cp_async_commit();
-  if (ngroups > 1) {
-    step_pools(irow, k, 1, t, lane, pn);
-    gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl, t, k, 1);
+  if constexpr (NST == 3) {
+    if (ngroups > 1) {
+      step_pools(irow, k, 1, t, lane, pn);
+      gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl, t, k, 1);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
 
   int stage = 0;
   for (int grp = 0; grp < ngroups; ++grp) {
     int pf[4] = {-1, -1, -1, -1};
     {
-      const int nx = grp + 2;
+      const int nx = grp + NST - 1;
       if (nx < ngroups) {
         step_pools(irow, k, nx, t, lane, pf);
-        const int st = stage + 2 >= 3 ? stage - 1 : stage + 2;
+        const int st = stage + NST - 1 >= NST ? stage - 1 : stage + NST - 1;
         gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl, t, k, nx);
       }
       cp_async_commit();
@@ -201,10 +203,14 @@ __global__ void __launch_bounds__(128) attn_fwd_bf16_kernel(const __nv_bfloat16*
     __syncwarp();
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) {
-      pc[s4] = pn[s4];
-      pn[s4] = pf[s4];
+      if constexpr (NST == 3) {
+        pc[s4] = pn[s4];
+        pn[s4] = pf[s4];
+      } else {
+        pc[s4] = pf[s4];
+      }
     }
-    stage = stage == 2 ? 0 : stage + 1;
+    stage = stage == NST - 1 ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 
@@ -322,6 +328,13 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const float* __restri
   for (int h = tid; h < Hq; h += blockDim.x) LSE[t * Hq + h] = ms[h] + logf(ls[h]);
 }
 
+// Gather stages per warp and CTAs per SM the kernel is compiled for.  Two
+// stages (16 KB per warp) with registers capped for three 4-warp CTAs per SM
+// measured 11.0 ms at L=131072, against 12.4 ms for three stages at two CTAs
+// per SM: more warps hide more of the MMA and softmax latency.
+constexpr int kFwdStages = 2;
+constexpr int kFwdMinBlocks = 3;
+
 cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
                                  const void* v, const int32_t* idx, void* o, float* lse, cudaStream_t s) {
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -332,15 +345,19 @@ cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, c
   auto vp = static_cast<const __nv_bfloat16*>(v);
   auto op = static_cast<__nv_bfloat16*>(o);
   if (d == 128) {
-    constexpr int smem = FwdCfg<128>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = FwdCfg<128, kFwdStages>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<128, kFwdStages, kFwdMinBlocks>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attn_fwd_bf16_kernel<128><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
+    attn_fwd_bf16_kernel<128, kFwdStages, kFwdMinBlocks>
+        <<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
   } else if (d == 64) {
-    constexpr int smem = FwdCfg<64>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int smem = FwdCfg<64, kFwdStages>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<64, kFwdStages, kFwdMinBlocks>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attn_fwd_bf16_kernel<64><<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
+    attn_fwd_bf16_kernel<64, kFwdStages, kFwdMinBlocks>
+        <<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
   } else {
     return cudaErrorNotSupported;
   }

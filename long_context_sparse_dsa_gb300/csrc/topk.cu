@@ -15,8 +15,9 @@
 //
 // One CTA of kTopkThreads threads per row, one read of the row in the
 // common case:
-//   1. 1024 evenly spaced samples give a threshold tau: the r-th largest
-//      sample, r = mu + 4 sqrt(mu) + 2 with mu = k * 1024 / n the expected
+//   1. 1024 evenly spaced samples give a threshold tau: the lower edge of the
+//      22-bit key bin of the r-th largest sample (two radix rounds),
+//      r = mu + 4 sqrt(mu) + 2 with mu = k * 1024 / n the expected
 //      number of samples at or above the k-th score, so that tau lies below
 //      the k-th score with high probability while few scores pass it (rows of
 //      at most kCandCap scores skip this and keep every score);
@@ -107,8 +108,11 @@ __device__ __forceinline__ void find_bin(const int* hist, int nbins, int need, i
   __syncthreads();
 }
 
-// Exact `need`-th largest key among keys[0..m) (need <= m): three radix
-// rounds.  Returns the key T; *above = how many keys are > T.
+// `need`-th largest key among keys[0..m) (need <= m) by radix rounds of
+// 11, 11 and 10 bits.  With ROUNDS = 3 it returns that key exactly and sets
+// *above = how many keys are > it.  With ROUNDS = 2 it returns the lower edge
+// of the 22-bit bin holding that key (a threshold at or below it).
+template <int ROUNDS = 3>
 __device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int need, int* hist, int* warp_buf,
                                                int* sel, int* above) {
   const int m_round = (m + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
@@ -117,7 +121,7 @@ __device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int 
   const int shifts[3] = {21, 10, 0};
   const int widths[3] = {11, 11, 10};
 #pragma unroll
-  for (int round = 0; round < 3; ++round) {
+  for (int round = 0; round < ROUNDS; ++round) {
     const int nb = 1 << widths[round];
     for (int b = threadIdx.x; b < nb; b += kTopkThreads) hist[b] = 0;
     __syncthreads();
@@ -139,7 +143,7 @@ __device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int 
     got_above += sel[1];
   }
   *above = got_above;
-  return prefix;
+  return ROUNDS == 3 ? prefix : (prefix << 10);
 }
 
 // One tile of the ordered selection: keep keys > T and the first `need_eq`
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     int rank = (int)(mu + 4.f * sqrtf(mu)) + 2;
     if (rank > kSamples) rank = kSamples;
     int above_s;
-    tau = select_kth(samples, kSamples, rank, hist, warp_buf, sel, &above_s);
+    tau = select_kth<2>(samples, kSamples, rank, hist, warp_buf, sel, &above_s);
   }
 
   // ---- 2. one pass: warp-segmented ordered compaction of keys >= tau -------
