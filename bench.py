@@ -118,13 +118,19 @@ def algorithmic(wl):
     partial = torch.where(t % 4 == 3, 0.0, t % 4 + 1)
     nkeys = float((4 * torch.minimum(elig, torch.tensor(float(k))) + partial).sum())
     eb = 2 if wl.dtype == "bf16" else 4
+    # with a backward the forward also writes the fp32 output (o_acc) and the
+    # backward reads it instead of re-forming D from K and V
+    acc = 4.0 * L * Hq * d if wl.passes == "fwd+bwd" else 0.0
     return {
         "pool_keys": {"bytes": L * di * eb + P * di * eb},
         "indexer": {"flops": 2.0 * Hi * di * pairs, "score_bytes": 4.0 * pairs},
         "topk": {"bytes": 4.0 * pairs + 4.0 * L * k},
-        "attn_fwd": {"bytes": nkeys * 2 * d * eb + L * Hq * d * eb * 2 + L * k * 4 + L * Hq * 4,
-                     "flops": 4.0 * Hq * d * nkeys},
-        "attn_bwd": {"bytes": nkeys * 2 * d * eb + nkeys * 2 * d * 4 + L * Hq * d * (3 * eb + 4) + L * k * 4,
+        # gathered K and V rows; Q read, O written, idx read, LSE written
+        "attn_fwd": {"bytes": nkeys * 2 * d * eb + L * Hq * d * eb * 2 + L * k * 4 + L * Hq * 4 + acc,
+                     "flops": (6.0 if acc else 4.0) * Hq * d * nkeys},
+        # gathered K and V rows, fp32 dK and dV reductions; Q, dO, o_acc read, dQ written; idx, LSE read
+        "attn_bwd": {"bytes": nkeys * 2 * d * eb + nkeys * 2 * d * 4 + L * Hq * d * (2 * eb + 4) + acc
+                     + L * k * 4 + L * Hq * 4,
                      "flops": 10.0 * Hq * d * nkeys},
         "nkeys": nkeys, "pairs": pairs,
     }
@@ -164,17 +170,19 @@ def run_ours(args, rank, world):
     host = dsa_inputs.make(wl, names, pin=True)
     d_in = {n: host[n].to(dev, non_blocking=True) for n in names}
     dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
-    bufs = dsa.alloc_forward_buffers(dims, dev)
+    # with a backward, the forward keeps its fp32 output for it (the backward
+    # then forms D from it and needs no workspace)
+    bufs = dsa.alloc_forward_buffers(dims, dev, o_acc=with_bwd)
     dq = torch.empty((wl.L, wl.Hq, wl.d), device=dev) if with_bwd else None
     dk = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
     dv = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
-    bws = dsa.alloc_backward_workspace(dims, dev) if with_bwd else None
+    bws = None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
     stream = torch.cuda.current_stream(dev)
     scores = bufs.ws.view(torch.float32)
     C = wl.q_chunk
     chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
-    launches_per_step = 1 + 2 * len(chunks) + 1 + (2 if with_bwd else 0)
+    launches_per_step = 1 + 2 * len(chunks) + 1 + (1 if with_bwd else 0)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -197,13 +205,14 @@ def run_ours(args, rank, world):
             if timers is not None:
                 marks.append(("topk", timers.pop()))
                 marks[-1][1].record(stream)
-        dsa.sparse_attn_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, stream)
+        dsa.sparse_attn_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, stream,
+                            o_acc=bufs.o_acc)
         if timers is not None:
             marks.append(("attn_fwd", timers.pop()))
             marks[-1][1].record(stream)
         if with_bwd:
             dsa.sparse_attn_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq,
-                                dk, dv, bws, None, stream)
+                                dk, dv, bws, None, stream, o_acc=bufs.o_acc)
             if timers is not None:
                 marks.append(("attn_bwd", timers.pop()))
                 marks[-1][1].record(stream)
@@ -299,10 +308,10 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
         for n in names:
             d_in[n].copy_(host[n], non_blocking=True)
         dsa.layer_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], d_in["q_I"], d_in["k_I"], d_in["w"], bufs.o, bufs.lse,
-                      bufs.idx, bufs.kpool, bufs.ws, stream=stream)
+                      bufs.idx, bufs.kpool, bufs.ws, stream=stream, o_acc=bufs.o_acc)
         if with_bwd:
             dsa.layer_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq, dk, dv,
-                          bws, stream=stream)
+                          bws, stream=stream, o_acc=bufs.o_acc)
         for src, dst in zip(outs, pinned_out):
             dst.copy_(src, non_blocking=True)
 

@@ -117,10 +117,11 @@ dsa_status dsa_validate_dims(const dsa_dims *dims, int32_t with_backward);
  * dims are invalid. */
 size_t dsa_workspace_bytes(const dsa_dims *dims);
 
-/* Bytes of device workspace dsa_sparse_attn_bwd / dsa_layer_bwd need: one
- * fp32 value per (query, head), L * Hq * 4 bytes, rounded up to 256 (it holds
- * D[t,h] = dO[t,h] . O[t,h] between the backward's two kernels).  Returns 0
- * if dims are invalid for a backward. */
+/* Bytes of device workspace dsa_sparse_attn_bwd / dsa_layer_bwd need when
+ * they are called without o_acc: one fp32 value per (query, head),
+ * L * Hq * 4 bytes, rounded up to 256 (it holds D[t,h] = dO[t,h] . O[t,h]
+ * between the backward's two kernels).  Returns 0 if dims are invalid for a
+ * backward. */
 size_t dsa_bwd_workspace_bytes(const dsa_dims *dims);
 
 /* Pool keys.  Page "SkyRL extends GLM-5.3-Flash ...", section "Model and
@@ -159,42 +160,54 @@ dsa_status dsa_topk(const dsa_dims *dims, const float *scores, int64_t q_begin, 
 
 /* Sparse attention forward over keys(t).  Same page, "1. DSA truly sparse"
  * (sparse kernel, NoPE, 2051 keys).  One K/V head shared by all Hq heads.
- *   q    [L, Hq, d]  layer dtype        k, v [L, d] layer dtype
- *   idx  [L, k]      int32 (from dsa_topk or the caller; entries < 0 skipped)
- *   o    [L, Hq, d]  layer dtype, output
- *   lse  [L, Hq]     fp32, output (natural log) */
+ *   q     [L, Hq, d]  layer dtype        k, v [L, d] layer dtype
+ *   idx   [L, k]      int32 (from dsa_topk or the caller; entries < 0 skipped)
+ *   o     [L, Hq, d]  layer dtype, output
+ *   lse   [L, Hq]     fp32, output (natural log)
+ *   o_acc [L, Hq, d]  fp32, optional output (NULL: not written), 16-byte
+ *                     aligned.  O before the cast to the layer dtype, with the
+ *                     softmax probabilities entering P.V as bf16 hi + lo parts
+ *                     (about 2^-17 relative instead of bf16's 2^-9).  Handing
+ *                     it to the backward replaces the backward's D
+ *                     recomputation pass; keeping it costs L*Hq*d*4 bytes. */
 dsa_status dsa_sparse_attn_fwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
-                               const int32_t *idx, void *o, float *lse, dsa_stream_t stream);
+                               const int32_t *idx, void *o, float *lse, float *o_acc, dsa_stream_t stream);
 
 /* Sparse attention backward (bf16 only).  Given dO, writes
  *   dq [L, Hq, d] fp32 (overwritten), dk, dv [L, d] fp32 (zeroed on the
  *   stream, then accumulated with fp32 atomics).
- * o and lse must be the forward's outputs for the same q, k, v, idx.  The
- * kernels form D = dO . O as sum_j P_j dP_j from the exact P and dP (a first
- * kernel, into ws), so the bf16 rounding of o does not enter the gradients;
- * o itself is validated but not read.  The selection is piecewise constant:
- * no gradient reaches the indexer inputs.
- *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory (scratch) */
+ * o, lse and o_acc must be the forward's outputs for the same q, k, v, idx.
+ * The bf16 rounding of o would enter every gradient through D = dO . O, so o
+ * is validated but not read.  With o_acc (non-NULL, 16-byte aligned) D is
+ * dO . o_acc, formed inside the gradient kernel, and ws is not used (may be
+ * NULL).  Without it a first kernel forms D = sum_j P_j dP_j from the
+ * recomputed P and dP into ws.  The selection is piecewise constant: no
+ * gradient reaches the indexer inputs.
+ *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory (scratch),
+ *        required when o_acc is NULL */
 dsa_status dsa_sparse_attn_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
-                               const int32_t *idx, const void *o, const float *lse, const void *dout,
-                               float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                               const int32_t *idx, const void *o, const float *lse, const float *o_acc,
+                               const void *dout, float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
                                dsa_stream_t stream);
 
 /* Whole forward: dsa_pool_keys once, then per chunk of q_chunk queries
  * dsa_indexer_score -> dsa_topk into the workspace, then dsa_sparse_attn_fwd.
- *   outputs: o [L,Hq,d], lse [L,Hq], idx [L,k], kpool [L/4,di]
+ *   outputs: o [L,Hq,d], lse [L,Hq], idx [L,k], kpool [L/4,di];
+ *            o_acc [L,Hq,d] fp32 when non-NULL (as in dsa_sparse_attn_fwd)
  *   ws      >= dsa_workspace_bytes(dims) bytes of device memory */
 dsa_status dsa_layer_fwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
                          const void *q_idx, const void *k_idx, const float *w,
-                         void *o, float *lse, int32_t *idx, void *kpool,
+                         void *o, float *lse, float *o_acc, int32_t *idx, void *kpool,
                          void *ws, size_t ws_bytes, dsa_stream_t stream);
 
-/* Whole backward: dsa_sparse_attn_bwd with the idx and lse the forward
- * saved (the indexer is not recomputed and gets no gradient).
- *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory */
+/* Whole backward: dsa_sparse_attn_bwd with the idx, lse and (optionally)
+ * o_acc the forward saved (the indexer is not recomputed and gets no gradient).
+ *   ws   >= dsa_bwd_workspace_bytes(dims) bytes of device memory when o_acc
+ *        is NULL; unused otherwise */
 dsa_status dsa_layer_bwd(const dsa_dims *dims, const void *q, const void *k, const void *v,
-                         const int32_t *idx, const void *o, const float *lse, const void *dout,
-                         float *dq, float *dk, float *dv, void *ws, size_t ws_bytes, dsa_stream_t stream);
+                         const int32_t *idx, const void *o, const float *lse, const float *o_acc,
+                         const void *dout, float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                         dsa_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error word that the
  * kernels set instead of trapping.  Returns DSA_OK, DSA_ERR_TIMEOUT (a
@@ -217,7 +230,8 @@ void dsa_set_wait_limit(uint32_t spins);
  * has no workspace argument, or a code path where a cudaMalloc (which may
  * synchronise the device) is not allowed.  The paper has no counterpart; it
  * is an interface convenience.
- *   Same arguments and outputs as dsa_layer_fwd, minus ws/ws_bytes.  The
+ *   Same arguments and outputs as dsa_layer_fwd, minus ws/ws_bytes and
+ *   o_acc (this entry point does not write one).  The
  *   indexer's score block lives in one fixed device array of
  *   DSA_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU that loads the
  *   library holds until the process exits; the query chunk is shrunk to

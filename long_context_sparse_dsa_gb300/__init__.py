@@ -66,10 +66,10 @@ def _load():
             "dsa_pool_keys": ([D, P, P, P], ctypes.c_int),
             "dsa_indexer_score": ([D, P, P, P, i64, i64, P, P], ctypes.c_int),
             "dsa_topk": ([D, P, i64, i64, P, P], ctypes.c_int),
-            "dsa_sparse_attn_fwd": ([D, P, P, P, P, P, P, P], ctypes.c_int),
-            "dsa_sparse_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
-            "dsa_layer_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
-            "dsa_layer_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_sparse_attn_fwd": ([D, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "dsa_sparse_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_layer_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_layer_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_fwd_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
@@ -150,24 +150,26 @@ def topk(dims, scores, q_begin, q_count, idx, stream=None):
                             _stream(stream)), "dsa_topk")
 
 
-def sparse_attn_fwd(dims, q, k, v, idx, o, lse, stream=None):
+def sparse_attn_fwd(dims, q, k, v, idx, o, lse, stream=None, o_acc=None):
+    """o_acc: optional fp32 [L, Hq, d] output (O with P carried beyond bf16)."""
     _check(_load().dsa_sparse_attn_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
-                                       _stream(stream)), "dsa_sparse_attn_fwd")
+                                       _ptr(o_acc), _stream(stream)), "dsa_sparse_attn_fwd")
 
 
-def sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None):
+def sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None, o_acc=None):
+    """With o_acc (the forward's) the workspace is not needed."""
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_sparse_attn_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
-                                       _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
+                                       _ptr(o_acc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                        _stream(stream)), "dsa_sparse_attn_bwd")
 
 
-def layer_fwd(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, ws, ws_bytes=None, stream=None):
+def layer_fwd(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, ws, ws_bytes=None, stream=None, o_acc=None):
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_layer_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(w),
-                                 _ptr(o), _ptr(lse), _ptr(idx), _ptr(kpool), _ptr(ws), int(ws_bytes),
+                                 _ptr(o), _ptr(lse), _ptr(o_acc), _ptr(idx), _ptr(kpool), _ptr(ws), int(ws_bytes),
                                  _stream(stream)), "dsa_layer_fwd")
 
 
@@ -178,11 +180,11 @@ def layer_fwd_noalloc(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, stream
            "dsa_layer_fwd_noalloc")
 
 
-def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None):
+def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=None, stream=None, o_acc=None):
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_layer_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
-                                 _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
+                                 _ptr(o_acc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                  _stream(stream)), "dsa_layer_bwd")
 
 
@@ -206,6 +208,7 @@ class LayerBuffers:
     idx: object
     kpool: object
     ws: object
+    o_acc: object = None
 
 
 def alloc_backward_workspace(dims: Dims, device="cuda"):
@@ -216,7 +219,8 @@ def alloc_backward_workspace(dims: Dims, device="cuda"):
     return torch.empty((n,), dtype=torch.uint8, device=device)
 
 
-def alloc_forward_buffers(dims: Dims, device="cuda") -> LayerBuffers:
+def alloc_forward_buffers(dims: Dims, device="cuda", o_acc: bool = False) -> LayerBuffers:
+    """o_acc=True adds the fp32 [L, Hq, d] output the backward can take in place of its D pass."""
     import torch
     dt = torch.bfloat16 if dims.dtype == DSA_BF16 else torch.float32
     ws_bytes = workspace_bytes(dims)
@@ -228,4 +232,5 @@ def alloc_forward_buffers(dims: Dims, device="cuda") -> LayerBuffers:
         idx=torch.empty((dims.L, dims.k), dtype=torch.int32, device=device),
         kpool=torch.empty((dims.L // 4, dims.di), dtype=dt, device=device),
         ws=torch.empty((ws_bytes,), dtype=torch.uint8, device=device),
+        o_acc=torch.empty((dims.L, dims.Hq, dims.d), dtype=torch.float32, device=device) if o_acc else None,
     )

@@ -117,14 +117,18 @@ dsa_status do_topk(const dsa_dims* d, const float* scores, int64_t q_begin, int6
 }
 
 dsa_status do_fwd(const dsa_dims* d, const void* q, const void* k, const void* v, const int32_t* idx, void* o,
-                  float* lse, cudaStream_t s) {
+                  float* lse, float* o_acc, cudaStream_t s) {
   cudaError_t e;
-  if (is_bf16(d))
-    e = dsa::launch_attn_fwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, s);
-  else
+  if (is_bf16(d)) {
+    e = dsa::launch_attn_fwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, o_acc, s);
+  } else {
     e = dsa::launch_attn_fwd_f32(d->L, d->Hq, d->d, d->k, d->scale, static_cast<const float*>(q),
                                  static_cast<const float*>(k), static_cast<const float*>(v), idx,
                                  static_cast<float*>(o), lse, s);
+    // an fp32 layer's output already carries P in fp32
+    if (e == cudaSuccess && o_acc != nullptr)
+      e = cudaMemcpyAsync(o_acc, o, (size_t)d->L * d->Hq * d->d * sizeof(float), cudaMemcpyDeviceToDevice, s);
+  }
   return cuda_status(e, "sparse_attn_fwd launch");
 }
 
@@ -134,12 +138,14 @@ size_t bwd_ws_bytes(const dsa_dims* d) {
 }
 
 dsa_status do_bwd(const dsa_dims* d, const void* q, const void* k, const void* v, const int32_t* idx,
-                  const float* lse, const void* dout, float* dq, float* dk, float* dv, float* dbuf, cudaStream_t s) {
+                  const float* lse, const float* o_acc, const void* dout, float* dq, float* dk, float* dv,
+                  float* dbuf, cudaStream_t s) {
   const size_t kv_bytes = (size_t)d->L * d->d * sizeof(float);
   cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, s);
   if (e != cudaSuccess) return cuda_status(e, "zeroing dk/dv");
-  e = dsa::launch_attn_bwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, lse, dout, dbuf, dq, dk, dv, s);
+  e = dsa::launch_attn_bwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, lse, dout, o_acc, dbuf, dq, dk,
+                                dv, s);
   return cuda_status(e, "sparse_attn_bwd launch");
 }
 
@@ -215,7 +221,7 @@ dsa_status dsa_topk(const dsa_dims* dims, const float* scores, int64_t q_begin, 
 }
 
 dsa_status dsa_sparse_attn_fwd(const dsa_dims* dims, const void* q, const void* k, const void* v,
-                               const int32_t* idx, void* o, float* lse, dsa_stream_t stream) {
+                               const int32_t* idx, void* o, float* lse, float* o_acc, dsa_stream_t stream) {
   g_msg[0] = 0;
   dsa_status st = check_dims(dims, false);
   if (st) return st;
@@ -225,7 +231,8 @@ dsa_status dsa_sparse_attn_fwd(const dsa_dims* dims, const void* q, const void* 
   REQUIRE_PTR(idx);
   REQUIRE_PTR(o);
   REQUIRE_PTR(lse);
-  return do_fwd(dims, q, k, v, idx, o, lse, (cudaStream_t)stream);
+  if (o_acc != nullptr && !aligned16(o_acc)) return fail(DSA_ERR_INVALID_ARG, "o_acc is not 16-byte aligned");
+  return do_fwd(dims, q, k, v, idx, o, lse, o_acc, (cudaStream_t)stream);
 }
 
 size_t dsa_bwd_workspace_bytes(const dsa_dims* dims) {
@@ -234,8 +241,9 @@ size_t dsa_bwd_workspace_bytes(const dsa_dims* dims) {
 }
 
 dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* k, const void* v,
-                               const int32_t* idx, const void* o, const float* lse, const void* dout, float* dq,
-                               float* dk, float* dv, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+                               const int32_t* idx, const void* o, const float* lse, const float* o_acc,
+                               const void* dout, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
+                               dsa_stream_t stream) {
   g_msg[0] = 0;
   dsa_status st = check_dims(dims, true);
   if (st) return st;
@@ -250,16 +258,20 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* 
   REQUIRE_PTR(dk);
   REQUIRE_PTR(dv);
   if (dk == dv) return fail(DSA_ERR_INVALID_ARG, "dk and dv must not alias");
+  if (o_acc != nullptr) {
+    if (!aligned16(o_acc)) return fail(DSA_ERR_INVALID_ARG, "o_acc is not 16-byte aligned");
+    return do_bwd(dims, q, k, v, idx, lse, o_acc, dout, dq, dk, dv, nullptr, (cudaStream_t)stream);
+  }
   const size_t need = bwd_ws_bytes(dims);
   if (ws == nullptr || ws_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "backward workspace of %zu bytes given, %zu needed", ws_bytes, need);
   if (!aligned16(ws)) return fail(DSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
-  return do_bwd(dims, q, k, v, idx, lse, dout, dq, dk, dv, static_cast<float*>(ws), (cudaStream_t)stream);
+  return do_bwd(dims, q, k, v, idx, lse, nullptr, dout, dq, dk, dv, static_cast<float*>(ws), (cudaStream_t)stream);
 }
 
 dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, const void* v, const void* q_idx,
-                         const void* k_idx, const float* w, void* o, float* lse, int32_t* idx, void* kpool,
-                         void* ws, size_t ws_bytes, dsa_stream_t stream) {
+                         const void* k_idx, const float* w, void* o, float* lse, float* o_acc, int32_t* idx,
+                         void* kpool, void* ws, size_t ws_bytes, dsa_stream_t stream) {
   g_msg[0] = 0;
   dsa_status st = check_dims(dims, false);
   if (st) return st;
@@ -273,6 +285,7 @@ dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, con
   REQUIRE_PTR(lse);
   REQUIRE_PTR(idx);
   REQUIRE_PTR(kpool);
+  if (o_acc != nullptr && !aligned16(o_acc)) return fail(DSA_ERR_INVALID_ARG, "o_acc is not 16-byte aligned");
   const size_t need = dsa_workspace_bytes(dims);
   if (ws == nullptr || ws_bytes < need)
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", ws_bytes, need);
@@ -286,13 +299,13 @@ dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, con
     if ((st = do_score(dims, q_idx, kpool, w, q0, n, scores, s))) return st;
     if ((st = do_topk(dims, scores, q0, n, idx, s))) return st;
   }
-  return do_fwd(dims, q, k, v, idx, o, lse, s);
+  return do_fwd(dims, q, k, v, idx, o, lse, o_acc, s);
 }
 
 dsa_status dsa_layer_bwd(const dsa_dims* dims, const void* q, const void* k, const void* v, const int32_t* idx,
-                         const void* o, const float* lse, const void* dout, float* dq, float* dk, float* dv,
-                         void* ws, size_t ws_bytes, dsa_stream_t stream) {
-  return dsa_sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws, ws_bytes, stream);
+                         const void* o, const float* lse, const float* o_acc, const void* dout, float* dq,
+                         float* dk, float* dv, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  return dsa_sparse_attn_bwd(dims, q, k, v, idx, o, lse, o_acc, dout, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 dsa_status dsa_check_device_error(dsa_stream_t stream) {

@@ -15,6 +15,8 @@
 // gather pipeline as the forward.  The first forms D[t,h] = sum_j P_j dP_j
 // into a [L, Hq] fp32 workspace; the second does everything else, so the
 // atomic traffic of the second is not interleaved with a pass that has none.
+// When the forward kept its output in fp32 with P carried beyond bf16 (o_acc),
+// the second kernel forms D = dO . o_acc itself and the first is not launched.
 // dQ stays in registers for the whole query.  Per 16-key step
 // the warp computes the 16x16 S and dP tiles with m16n8k16 MMAs (heads on M),
 // then the 16-key x d tiles of dK and dV with the keys on M: the transposed
@@ -60,8 +62,8 @@ template <int D, int PASS>
 __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
     const int32_t* __restrict__ idx, const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ dO,
-    float* __restrict__ Dbuf, float* __restrict__ dQ, float* __restrict__ dK, float* __restrict__ dV, int64_t L,
-    int Hq, int k, float scale, float scale_log2) {
+    const float* __restrict__ Oacc, float* __restrict__ Dbuf, float* __restrict__ dQ, float* __restrict__ dK,
+    float* __restrict__ dV, int64_t L, int Hq, int k, float scale, float scale_log2) {
   using C = BwdCfg<D, PASS>;
   extern __shared__ __align__(128) unsigned char bwd_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,8 +136,34 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
   if (PASS == 2) {
-    Dg = __ldg(Dbuf + row0 + g);
-    Dg8 = __ldg(Dbuf + row0 + g + 8);
+    if (Oacc != nullptr) {
+      // D = dO . O over this lane's dO fragment columns (ks*16 + 2qi + {0,1}
+      // and ks*16 + 8 + 2qi + {0,1}), then summed over the quad
+      const float* a0 = Oacc + (row0 + g) * D + 2 * qi;
+      const float* a8 = a0 + 8 * D;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const float2 x0 = __ldg(reinterpret_cast<const float2*>(a0 + ks * 16));
+        const float2 x1 = __ldg(reinterpret_cast<const float2*>(a0 + ks * 16 + 8));
+        const float2 y0 = __ldg(reinterpret_cast<const float2*>(a8 + ks * 16));
+        const float2 y1 = __ldg(reinterpret_cast<const float2*>(a8 + ks * 16 + 8));
+        Dg = fmaf(__uint_as_float(da[ks][0] << 16), x0.x, Dg);
+        Dg = fmaf(__uint_as_float(da[ks][0] & 0xFFFF0000u), x0.y, Dg);
+        Dg = fmaf(__uint_as_float(da[ks][2] << 16), x1.x, Dg);
+        Dg = fmaf(__uint_as_float(da[ks][2] & 0xFFFF0000u), x1.y, Dg);
+        Dg8 = fmaf(__uint_as_float(da[ks][1] << 16), y0.x, Dg8);
+        Dg8 = fmaf(__uint_as_float(da[ks][1] & 0xFFFF0000u), y0.y, Dg8);
+        Dg8 = fmaf(__uint_as_float(da[ks][3] << 16), y1.x, Dg8);
+        Dg8 = fmaf(__uint_as_float(da[ks][3] & 0xFFFF0000u), y1.y, Dg8);
+      }
+      Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
+      Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);
+      Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 1);
+      Dg8 += __shfl_xor_sync(0xffffffffu, Dg8, 2);
+    } else {
+      Dg = __ldg(Dbuf + row0 + g);
+      Dg8 = __ldg(Dbuf + row0 + g + 8);
+    }
   }
 
   for (int step = 0; step < nsteps; ++step) {
@@ -336,8 +364,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 template <int D, int PASS>
 static cudaError_t launch_pass(int64_t L, int Hq, int k, float scale, const __nv_bfloat16* q, const __nv_bfloat16* kk,
                                const __nv_bfloat16* v, const int32_t* idx, const float* lse,
-                               const __nv_bfloat16* dout, float* dbuf, float* dq, float* dk, float* dv,
-                               cudaStream_t s) {
+                               const __nv_bfloat16* dout, const float* oacc, float* dbuf, float* dq, float* dk,
+                               float* dv, cudaStream_t s) {
   using C = BwdCfg<D, PASS>;
   const float scale_log2 = scale * 1.4426950408889634f;
   const int64_t items = L * (Hq / 16);
@@ -346,28 +374,31 @@ static cudaError_t launch_pass(int64_t L, int Hq, int k, float scale, const __nv
                                        C::SMEM);
   if (e != cudaSuccess) return e;
   attn_bwd_bf16_kernel<D, PASS><<<(unsigned)blocks, 32 * C::WARPS, C::SMEM, s>>>(
-      q, kk, v, idx, lse, dout, dbuf, dq, dk, dv, L, Hq, k, scale, scale_log2);
+      q, kk, v, idx, lse, dout, oacc, dbuf, dq, dk, dv, L, Hq, k, scale, scale_log2);
   return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_passes(int64_t L, int Hq, int k, float scale, const __nv_bfloat16* q,
+                                 const __nv_bfloat16* kk, const __nv_bfloat16* v, const int32_t* idx,
+                                 const float* lse, const __nv_bfloat16* dout, const float* oacc, float* dbuf,
+                                 float* dq, float* dk, float* dv, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (oacc == nullptr) e = launch_pass<D, 1>(L, Hq, k, scale, q, kk, v, idx, lse, dout, nullptr, dbuf, dq, dk, dv, s);
+  if (e == cudaSuccess) e = launch_pass<D, 2>(L, Hq, k, scale, q, kk, v, idx, lse, dout, oacc, dbuf, dq, dk, dv, s);
+  return e;
 }
 
 cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
                                  const void* v, const int32_t* idx, const float* lse, const void* dout,
-                                 float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s) {
+                                 const float* oacc, float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s) {
   auto qp = static_cast<const __nv_bfloat16*>(q);
   auto kp = static_cast<const __nv_bfloat16*>(kk);
   auto vp = static_cast<const __nv_bfloat16*>(v);
   auto gp = static_cast<const __nv_bfloat16*>(dout);
-  cudaError_t e;
-  if (d == 128) {
-    e = launch_pass<128, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
-    if (e == cudaSuccess) e = launch_pass<128, 2>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
-  } else if (d == 64) {
-    e = launch_pass<64, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
-    if (e == cudaSuccess) e = launch_pass<64, 2>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, dbuf, dq, dk, dv, s);
-  } else {
-    e = cudaErrorNotSupported;
-  }
-  return e;
+  if (d == 128) return launch_passes<128>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, oacc, dbuf, dq, dk, dv, s);
+  if (d == 64) return launch_passes<64>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, oacc, dbuf, dq, dk, dv, s);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace dsa

@@ -17,6 +17,11 @@
 // m16n8k16 bf16 MMAs: S = Q K^T and O += P V, fp32 accumulation, online
 // softmax in registers.  The kernel is bound by the L2->SM gather bandwidth
 // (about 16 flop per gathered byte), not by the MMAs.
+//
+// With an o_acc buffer (the ACC variant) the probabilities enter P V as two
+// bf16 terms, P = hi + lo with hi = bf16(P) and lo = bf16(P - hi), so the fp32
+// output carries P to about 2^-17 relative instead of bf16's 2^-9; o_acc then
+// gives the backward D = dO . O without a recomputation pass.
 #include "common.cuh"
 #include "gather.cuh"
 #include "launch.h"
@@ -33,13 +38,21 @@ struct FwdCfg {
   static constexpr int SMEM = WARPS * NST * STAGE_BYTES;
 };
 
-template <int D, int NST, int MINB>
+// x = hi + lo for two fp32 values: hi their bf16 rounding, lo the bf16
+// rounding of the (exact) fp32 remainder.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
+template <int D, int NST, int MINB, bool ACC>
 __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
                                                             const __nv_bfloat16* __restrict__ K,
                                                             const __nv_bfloat16* __restrict__ V,
                                                             const int32_t* __restrict__ idx,
                                                             __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
-                                                            int64_t L, int Hq, int k, float scale_log2) {
+                                                            float* __restrict__ Oacc, int64_t L, int Hq, int k,
+                                                            float scale_log2) {
   using C = FwdCfg<D, NST>;
   static_assert(NST == 2 || NST == 3, "the pool ring below is written for two or three stages");
   extern __shared__ __align__(128) unsigned char fwd_smem[];
@@ -186,8 +199,18 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
         o[n][3] *= a1;
       }
     }
-    const uint32_t pa0 = pack_bf16(s[0][0], s[0][1]), pa1 = pack_bf16(s[0][2], s[0][3]);
-    const uint32_t pa2 = pack_bf16(s[1][0], s[1][1]), pa3 = pack_bf16(s[1][2], s[1][3]);
+    uint32_t pa0, pa1, pa2, pa3, pl0 = 0, pl1 = 0, pl2 = 0, pl3 = 0;
+    if constexpr (ACC) {
+      split_bf16x2(s[0][0], s[0][1], pa0, pl0);
+      split_bf16x2(s[0][2], s[0][3], pa1, pl1);
+      split_bf16x2(s[1][0], s[1][1], pa2, pl2);
+      split_bf16x2(s[1][2], s[1][3], pa3, pl3);
+    } else {
+      pa0 = pack_bf16(s[0][0], s[0][1]);
+      pa1 = pack_bf16(s[0][2], s[0][3]);
+      pa2 = pack_bf16(s[1][0], s[1][1]);
+      pa3 = pack_bf16(s[1][2], s[1][3]);
+    }
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int key = (mtx & 1) * 8 + r;
@@ -198,6 +221,10 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
         ldsm_x4_t(vs_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, b0, b1);
         mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, b2, b3);
+        if constexpr (ACC) {
+          mma_bf16_16816(o[2 * j], pl0, pl1, pl2, pl3, b0, b1);
+          mma_bf16_16816(o[2 * j + 1], pl0, pl1, pl2, pl3, b2, b3);
+        }
       }
     }
     __syncwarp();
@@ -225,6 +252,15 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
   for (int n = 0; n < D / 8; ++n) {
     *reinterpret_cast<uint32_t*>(orow0 + n * 8 + 2 * qi) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
     *reinterpret_cast<uint32_t*>(orow1 + n * 8 + 2 * qi) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+  }
+  if constexpr (ACC) {
+    float* arow0 = Oacc + (t * Hq + hg * 16 + g) * D + 2 * qi;
+    float* arow1 = arow0 + 8 * D;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      __stcs(reinterpret_cast<float2*>(arow0 + n * 8), make_float2(o[n][0] * inv0, o[n][1] * inv0));
+      __stcs(reinterpret_cast<float2*>(arow1 + n * 8), make_float2(o[n][2] * inv1, o[n][3] * inv1));
+    }
   }
   if (qi == 0) {
     constexpr float kLn2 = 0.6931471805599453f;
@@ -335,8 +371,21 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const float* __restri
 constexpr int kFwdStages = 2;
 constexpr int kFwdMinBlocks = 3;
 
+template <int D, bool ACC>
+static cudaError_t launch_fwd(int64_t blocks, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                              const __nv_bfloat16* v, const int32_t* idx, __nv_bfloat16* o, float* lse,
+                              float* o_acc, int64_t L, int Hq, int kk, float scale_log2, cudaStream_t s) {
+  constexpr int smem = FwdCfg<D, kFwdStages>::SMEM;
+  auto kern = attn_fwd_bf16_kernel<D, kFwdStages, kFwdMinBlocks, ACC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)blocks, 128, smem, s>>>(q, k, v, idx, o, lse, o_acc, L, Hq, kk, scale_log2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
-                                 const void* v, const int32_t* idx, void* o, float* lse, cudaStream_t s) {
+                                 const void* v, const int32_t* idx, void* o, float* lse, float* o_acc,
+                                 cudaStream_t s) {
   const float scale_log2 = scale * 1.4426950408889634f;
   const int64_t items = L * (Hq / 16);
   const int64_t blocks = (items + 3) / 4;
@@ -344,24 +393,13 @@ cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, c
   auto kp = static_cast<const __nv_bfloat16*>(kk);
   auto vp = static_cast<const __nv_bfloat16*>(v);
   auto op = static_cast<__nv_bfloat16*>(o);
-  if (d == 128) {
-    constexpr int smem = FwdCfg<128, kFwdStages>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<128, kFwdStages, kFwdMinBlocks>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_fwd_bf16_kernel<128, kFwdStages, kFwdMinBlocks>
-        <<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
-  } else if (d == 64) {
-    constexpr int smem = FwdCfg<64, kFwdStages>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<64, kFwdStages, kFwdMinBlocks>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_fwd_bf16_kernel<64, kFwdStages, kFwdMinBlocks>
-        <<<(unsigned)blocks, 128, smem, s>>>(qp, kp, vp, idx, op, lse, L, Hq, k, scale_log2);
-  } else {
-    return cudaErrorNotSupported;
-  }
-  return cudaGetLastError();
+  if (d == 128)
+    return o_acc ? launch_fwd<128, true>(blocks, qp, kp, vp, idx, op, lse, o_acc, L, Hq, k, scale_log2, s)
+                 : launch_fwd<128, false>(blocks, qp, kp, vp, idx, op, lse, o_acc, L, Hq, k, scale_log2, s);
+  if (d == 64)
+    return o_acc ? launch_fwd<64, true>(blocks, qp, kp, vp, idx, op, lse, o_acc, L, Hq, k, scale_log2, s)
+                 : launch_fwd<64, false>(blocks, qp, kp, vp, idx, op, lse, o_acc, L, Hq, k, scale_log2, s);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_attn_fwd_f32(int64_t L, int Hq, int d, int k, float scale, const float* q, const float* kk,

@@ -25,17 +25,20 @@ cudaError_t launch_indexer_tc_bf16(int64_t L, int Hi, int di, const void* q_idx,
 cudaError_t launch_topk(int64_t L, int k, const float* scores, int64_t q_begin, int64_t q_count, int32_t* idx,
                         cudaStream_t s);
 
-// Sparse attention forward.
+// Sparse attention forward; o_acc (optional, fp32) gets O with P carried beyond bf16.
 cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
-                                 const void* v, const int32_t* idx, void* o, float* lse, cudaStream_t s);
+                                 const void* v, const int32_t* idx, void* o, float* lse, float* o_acc,
+                                 cudaStream_t s);
 cudaError_t launch_attn_fwd_f32(int64_t L, int Hq, int d, int k, float scale, const float* q, const float* kk,
                                 const float* v, const int32_t* idx, float* o, float* lse, cudaStream_t s);
 
 // Sparse attention backward (bf16): dq overwritten; dk, dv must be zeroed by the
-// caller; dbuf is an [L, Hq] fp32 workspace (D per query row).
+// caller.  With oacc (the forward's fp32 output) D = dO . oacc is formed in the
+// gradient kernel; without it dbuf, an [L, Hq] fp32 workspace, carries D from
+// a first kernel.
 cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
                                  const void* v, const int32_t* idx, const float* lse, const void* dout,
-                                 float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s);
+                                 const float* oacc, float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s);
 
 int device_sm_count();
 

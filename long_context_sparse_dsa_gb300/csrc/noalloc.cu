@@ -80,5 +80,5 @@ extern "C" dsa_status dsa_layer_fwd_noalloc(const dsa_dims* dims, const void* q,
     if ((st = dsa_indexer_score(dims, q_idx, kpool, w, q0, n, scores, stream)) != DSA_OK) return st;
     if ((st = dsa_topk(dims, scores, q0, n, idx, stream)) != DSA_OK) return st;
   }
-  return dsa_sparse_attn_fwd(dims, q, k, v, idx, o, lse, stream);
+  return dsa_sparse_attn_fwd(dims, q, k, v, idx, o, lse, nullptr, stream);
 }

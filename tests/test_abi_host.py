@@ -81,16 +81,26 @@ def test_null_and_misaligned_pointers_fail_before_launch(lib):
     assert lib.dsa_topk(ctypes.byref(d), 256, -1, 10, 256, None) == dsa.DSA_ERR_INVALID_ARG
     # too small a workspace is reported as such
     p = ctypes.c_void_p(256)
-    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, p, 16, None) == dsa.DSA_ERR_WORKSPACE
-    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, None, 1 << 40, None) == \
+    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, None, p, p, p, 16, None) == \
         dsa.DSA_ERR_WORKSPACE
-    # aliased gradient outputs
-    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, None, 0, None) == \
+    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, None, p, p, None, 1 << 40, None) == \
+        dsa.DSA_ERR_WORKSPACE
+    # the optional fp32 output is checked only when given
+    odd = ctypes.c_void_p(264)          # 8 mod 16
+    assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, odd, p, p, p, 16, None) == \
         dsa.DSA_ERR_INVALID_ARG
-    # the backward needs its D workspace
+    assert b"o_acc" in lib.dsa_last_error_message()
+    assert lib.dsa_sparse_attn_fwd(ctypes.byref(d), p, p, p, p, p, p, odd, None) == dsa.DSA_ERR_INVALID_ARG
+    # aliased gradient outputs
+    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, p, None, 0, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    # without o_acc the backward needs its D workspace; with a misaligned one it fails on that
     q = ctypes.c_void_p(512)
-    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, p, p, p, q, None, 0, None) == \
+    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, q, None, 0, None) == \
         dsa.DSA_ERR_WORKSPACE
+    assert lib.dsa_sparse_attn_bwd(ctypes.byref(d), p, p, p, p, p, p, odd, p, p, p, q, None, 0, None) == \
+        dsa.DSA_ERR_INVALID_ARG
+    assert b"o_acc" in lib.dsa_last_error_message()
     assert lib.dsa_selftest_bounded_wait(0, None) == dsa.DSA_ERR_INVALID_ARG
 
 

@@ -188,11 +188,23 @@ def test_attn_fwd_matches_oracle(dtype, Hq, d, k):
     Or, LSEr = oracle.attn_fwd(_f32(Q), _f32(K), _f32(V), idx, scale)
     assert np.abs(_f32(O) - Or).max() <= TOL[dtype]
     assert np.abs(lse.cpu().numpy() - LSEr).max() <= (1e-3 if dtype == "bf16" else 1e-4)
+    # with the fp32 output: O and LSE unchanged bit for bit (fp32 layers) or within
+    # tolerance (bf16: P.V now carries the low part of P), o_acc within 1e-4
+    O2, lse2 = torch.empty_like(O), torch.empty_like(lse)
+    o_acc = torch.full((L, Hq, d), float("nan"), device=DEV)
+    dsa.sparse_attn_fwd(dims, Q.to(DEV), K.to(DEV), V.to(DEV), torch.from_numpy(idx).to(DEV), O2, lse2, o_acc=o_acc)
+    dsa.check_device_error()
+    assert torch.equal(lse2, lse)
+    assert np.abs(_f32(O2) - Or).max() <= TOL[dtype]
+    assert np.abs(o_acc.cpu().numpy() - Or).max() <= 1e-4
+    if dtype == "fp32":
+        assert torch.equal(O2, O) and torch.equal(o_acc, O)
 
 
 @pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64)])
 @pytest.mark.parametrize("k", [3, 32])
-def test_attn_bwd_matches_oracle(Hq, d, k):
+@pytest.mark.parametrize("use_o_acc", [False, True])
+def test_attn_bwd_matches_oracle(Hq, d, k, use_o_acc):
     L = 1000
     Q, K, V, dO, idx = _attn_case(L, Hq, d, k, "bf16", seed=20 + k)
     scale = 1 / math.sqrt(d)
@@ -201,12 +213,13 @@ def test_attn_bwd_matches_oracle(Hq, d, k):
     idx_d = torch.from_numpy(idx).to(DEV)
     O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((L, Hq), device=DEV)
-    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse)
+    o_acc = torch.empty((L, Hq, d), device=DEV) if use_o_acc else None
+    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, o_acc=o_acc)
     dq = torch.empty((L, Hq, d), device=DEV)
     dk = torch.full((L, d), 5.0, device=DEV)     # must be overwritten, not accumulated into
     dv = torch.full((L, d), 5.0, device=DEV)
-    ws = dsa.alloc_backward_workspace(dims, DEV)
-    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws)
+    ws = None if use_o_acc else dsa.alloc_backward_workspace(dims, DEV)
+    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws, o_acc=o_acc)
     dsa.check_device_error()
     dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
     errs = {name: float(np.abs(got.cpu().numpy() - ref).max())

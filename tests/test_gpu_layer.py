@@ -2,7 +2,8 @@
 
 * the tiny fp32 workload (L=4096) in full: selection bit-exact, O/LSE 1e-4;
 * a bf16 layer with several indexer chunks, integer indexer inputs: selection
-  bit-exact for every row, O on sampled rows and dQ/dK/dV everywhere within 2e-2;
+  bit-exact for every row, O on sampled rows and dQ/dK/dV everywhere within 2e-2,
+  for the backward with its own D pass and with the forward's fp32 o_acc;
 * chunk-size invariance and run-to-run bitwise determinism of the forward;
 * the full-size workloads on sampled rows, with near-tie tolerance for the
   selection where scores come from N(0,1) inputs (fp32 scores are not
@@ -35,20 +36,23 @@ def _f32(t):
     return t.detach().to("cpu", torch.float32).numpy()
 
 
-def _run_layer(wl, host, with_bwd, q_chunk=None):
+def _run_layer(wl, host, with_bwd, q_chunk=None, o_acc=False):
+    """o_acc=True: the forward also writes the fp32 output and the backward takes
+    D from it (no workspace, no D pass), as the benchmark runs the layer."""
     dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=q_chunk or wl.q_chunk, scale=wl.scale,
                          dtype=wl.dtype)
     dev = {n: t.to(DEV) for n, t in host.items()}
-    bufs = dsa.alloc_forward_buffers(dims, DEV)
+    bufs = dsa.alloc_forward_buffers(dims, DEV, o_acc=o_acc)
     dsa.layer_fwd(dims, dev["Q"], dev["K"], dev["V"], dev["q_I"], dev["k_I"], dev["w"], bufs.o, bufs.lse, bufs.idx,
-                  bufs.kpool, bufs.ws)
-    out = {"o": bufs.o, "lse": bufs.lse, "idx": bufs.idx, "kpool": bufs.kpool}
+                  bufs.kpool, bufs.ws, o_acc=bufs.o_acc)
+    out = {"o": bufs.o, "lse": bufs.lse, "idx": bufs.idx, "kpool": bufs.kpool, "o_acc": bufs.o_acc}
     if with_bwd:
         dq = torch.empty((wl.L, wl.Hq, wl.d), device=DEV)
         dk = torch.empty((wl.L, wl.d), device=DEV)
         dv = torch.empty((wl.L, wl.d), device=DEV)
-        ws = dsa.alloc_backward_workspace(dims, DEV)
-        dsa.layer_bwd(dims, dev["Q"], dev["K"], dev["V"], bufs.idx, bufs.o, bufs.lse, dev["dO"], dq, dk, dv, ws)
+        ws = None if o_acc else dsa.alloc_backward_workspace(dims, DEV)
+        dsa.layer_bwd(dims, dev["Q"], dev["K"], dev["V"], bufs.idx, bufs.o, bufs.lse, dev["dO"], dq, dk, dv, ws,
+                      o_acc=bufs.o_acc)
         out.update(dq=dq, dk=dk, dv=dv)
     dsa.check_device_error()
     return out
@@ -76,20 +80,22 @@ def _bf16_multichunk():
 def test_bf16_layer_fwd_bwd_multichunk_integer_indexer():
     wl = _bf16_multichunk()
     host = dsa_inputs.make(wl)
-    out = _run_layer(wl, host, with_bwd=True)
     f = {n: _f32(t) for n, t in host.items()}
     kp = oracle.pool_keys(f["k_I"], True)
-    assert np.array_equal(_f32(out["kpool"]).view(np.uint32), kp.view(np.uint32))
     idx = oracle.select_rows(f["q_I"], kp, f["w"], wl.k, None, threads=NTHREADS)
-    assert np.array_equal(out["idx"].cpu().numpy(), idx)
     rows = dsa_inputs.sample_rows(wl, 192)
     O, LSE = oracle.attn_fwd(f["Q"], f["K"], f["V"], idx, wl.scale, rows)
-    assert np.abs(_f32(out["o"])[rows] - O).max() <= 2e-2
-    assert np.abs(out["lse"].cpu().numpy()[rows] - LSE).max() <= 1e-3
     dQ, dK, dV = oracle.attn_bwd(f["Q"], f["K"], f["V"], idx, f["dO"], wl.scale, threads=NTHREADS)
-    assert np.abs(out["dq"].cpu().numpy() - dQ).max() <= 2e-2
-    assert np.abs(out["dk"].cpu().numpy() - dK).max() <= 2e-2
-    assert np.abs(out["dv"].cpu().numpy() - dV).max() <= 2e-2
+    for o_acc in (False, True):
+        out = _run_layer(wl, host, with_bwd=True, o_acc=o_acc)
+        assert np.array_equal(_f32(out["kpool"]).view(np.uint32), kp.view(np.uint32))
+        assert np.array_equal(out["idx"].cpu().numpy(), idx)
+        assert np.abs(_f32(out["o"])[rows] - O).max() <= 2e-2
+        assert np.abs(out["lse"].cpu().numpy()[rows] - LSE).max() <= 1e-3
+        if o_acc:
+            assert np.abs(out["o_acc"].cpu().numpy()[rows] - O).max() <= 1e-4
+        errs = {n: float(np.abs(out[n].cpu().numpy() - ref).max()) for n, ref in (("dq", dQ), ("dk", dK), ("dv", dV))}
+        assert max(errs.values()) <= 2e-2, (o_acc, errs)
 
 
 def test_forward_is_chunk_invariant_and_deterministic():
@@ -133,7 +139,7 @@ def test_full_size_workload_sampled(name):
     wl = dsa_inputs.WORKLOADS[name]
     with_bwd = wl.passes == "fwd+bwd"
     host = dsa_inputs.make(wl, ("Q", "K", "V", "q_I", "k_I", "w") + (("dO",) if with_bwd else ()))
-    out = _run_layer(wl, host, with_bwd)
+    out = _run_layer(wl, host, with_bwd, o_acc=with_bwd)
     rows = np.asarray(dsa_inputs.sample_rows(wl, 96))
     f = {n: _f32(host[n]) for n in ("K", "V", "q_I", "k_I", "w")}
     kp = oracle.pool_keys(f["k_I"], True)
@@ -148,12 +154,13 @@ def test_full_size_workload_sampled(name):
     assert np.abs(_f32(out["o"][agree]) - O).max() <= 2e-2
     assert np.abs(out["lse"][agree].cpu().numpy() - LSE).max() <= 1e-3
     if with_bwd:
+        assert np.abs(out["o_acc"][agree].cpu().numpy() - O).max() <= 1e-4
         dOr = _f32(host["dO"][agree])
         dQ, _, _ = oracle.attn_bwd(Qr, f["K"], f["V"], idx_full, dOr, wl.scale, agree, with_dkv=False,
                                    threads=NTHREADS, q_compact=True)
         assert np.abs(out["dq"][agree].cpu().numpy() - dQ).max() <= 2e-2
         # closed forms valid at any size: sum_j dV[j] = sum_{t,h} dO[t,h] (softmax rows sum to 1) and
-        # sum_j dK[j] = 0 (sum_j dS = dO.O - D = 0), up to rounding (D uses the bf16-rounded O)
+        # sum_j dK[j] = 0 (sum_j dS = dO.O - D = 0), up to rounding
         dv_sum = out["dv"].double().sum(0).cpu().numpy()
         do_sum = host["dO"].to(torch.float64).sum((0, 1)).numpy()
         assert np.abs(dv_sum - do_sum).max() <= 1e-5 * wl.L * wl.Hq ** 0.5
