@@ -214,16 +214,23 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int key = (mtx & 1) * 8 + r;
+      // V fragments two 16-column blocks at a time: the four hi MMAs go before
+      // the four lo MMAs, so MMAs into the same accumulator are four apart
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
+      for (int j = 0; j < D / 16; j += 2) {
         const int ch = 2 * j + (mtx >> 1);
-        uint32_t b0, b1, b2, b3;
+        uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
         ldsm_x4_t(vs_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        ldsm_x4_t(vs_base + key * C::ROW_BYTES + (((ch + 2) ^ (key & 7)) << 4), c0, c1, c2, c3);
         mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, b0, b1);
         mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, b2, b3);
+        mma_bf16_16816(o[2 * j + 2], pa0, pa1, pa2, pa3, c0, c1);
+        mma_bf16_16816(o[2 * j + 3], pa0, pa1, pa2, pa3, c2, c3);
         if constexpr (ACC) {
           mma_bf16_16816(o[2 * j], pl0, pl1, pl2, pl3, b0, b1);
           mma_bf16_16816(o[2 * j + 1], pl0, pl1, pl2, pl3, b2, b3);
+          mma_bf16_16816(o[2 * j + 2], pl0, pl1, pl2, pl3, c0, c1);
+          mma_bf16_16816(o[2 * j + 3], pl0, pl1, pl2, pl3, c2, c3);
         }
       }
     }

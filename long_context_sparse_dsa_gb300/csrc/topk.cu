@@ -42,6 +42,7 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 4096;                        // candidate keys + indices in SMEM (32 KB)
 constexpr int kWarpCap = kCandCap / kTopkWarps;       // per-warp compaction region
 constexpr int kSamples = 1024;
+constexpr int kStreamUnroll = 4;                      // 128-score groups a warp loads per iteration
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -194,7 +195,8 @@ __device__ __forceinline__ void select_from_candidates(const uint32_t* cand_key,
   }
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
+// Shared memory (about 45 KB) allows five CTAs per SM; the register cap keeps that.
+__global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
                                                             int64_t q_begin, int64_t q_count,
                                                             int32_t* __restrict__ idx) {
   __shared__ int hist[2048];
@@ -235,6 +237,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   }
 
   // ---- 2. one pass: warp-segmented ordered compaction of keys >= tau -------
+  // A warp reads kStreamUnroll x 128 consecutive scores per iteration, all
+  // loads issued before the first compaction, so several of its loads are in
+  // flight at once; the 128-score groups are then compacted in index order.
   if (threadIdx.x == 0) flag_overflow = 0;
   const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 127) & ~127;   // multiple of 128 elements
   const int w_begin = wid * seg;
@@ -243,46 +248,53 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   bool overflow = false;
   uint32_t* my_key = cand_key + wid * kWarpCap;
   int32_t* my_idx = cand_idx + wid * kWarpCap;
-  for (int base = w_begin; base < w_end; base += 128) {
-    const int e = base + 4 * lane;
-    uint32_t kk[4];
-    if (vec4 && e + 3 < w_end) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + e));
-      kk[0] = order_key(f.x);
-      kk[1] = order_key(f.y);
-      kk[2] = order_key(f.z);
-      kk[3] = order_key(f.w);
-    } else {
+  for (int base = w_begin; base < w_end && !overflow; base += 128 * kStreamUnroll) {
+    uint32_t kk[kStreamUnroll][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kk[j] = (e + j < w_end) ? order_key(__ldg(row + e + j)) : 0u;
-    }
-    bool f[4];
-    int c = 0;
+    for (int u = 0; u < kStreamUnroll; ++u) {
+      const int e = base + u * 128 + 4 * lane;
+      if (vec4 && e + 3 < w_end) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row + e));
+        kk[u][0] = order_key(f.x);
+        kk[u][1] = order_key(f.y);
+        kk[u][2] = order_key(f.z);
+        kk[u][3] = order_key(f.w);
+      } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[j] = (e + j < w_end) && kk[j] >= tau;
-      c += f[j];
-    }
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-    if (wcount + tot > kWarpCap) {
-      overflow = true;
-      break;
-    }
-    int pos = wcount + incl - c;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (f[j]) {
-        my_key[pos] = kk[j];
-        my_idx[pos] = e + j;
-        ++pos;
+        for (int j = 0; j < 4; ++j) kk[u][j] = (e + j < w_end) ? order_key(__ldg(row + e + j)) : 0u;
       }
-    wcount += tot;
+    }
+#pragma unroll
+    for (int u = 0; u < kStreamUnroll; ++u) {
+      const int e = base + u * 128 + 4 * lane;
+      bool f[4];
+      int c = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[j] = (e + j < w_end) && kk[u][j] >= tau;
+        c += f[j];
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (overflow || wcount + tot > kWarpCap) {   // warp-uniform
+        overflow = true;
+        continue;
+      }
+      int pos = wcount + incl - c;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (f[j]) {
+          my_key[pos] = kk[u][j];
+          my_idx[pos] = e + j;
+          ++pos;
+        }
+      wcount += tot;
+    }
   }
   if (lane == 0) {
     warp_cnt[wid] = wcount;
@@ -293,29 +305,47 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   for (int w = 0; w < kTopkWarps; ++w) m += warp_cnt[w];
   const bool fast = !flag_overflow && m >= k;
   if (fast) {
-    // close the gaps between the warp regions (in warp order = index order)
-    int dst = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const int cnt = warp_cnt[w];
-      const int src = w * kWarpCap;
-      // src >= dst always; copy forward in chunks so overlapping moves stay correct
-      for (int i0 = 0; i0 < cnt; i0 += kTopkThreads) {
-        const int i = i0 + threadIdx.x;
-        uint32_t kv = 0;
-        int32_t iv = 0;
-        if (i < cnt) {
-          kv = cand_key[src + i];
-          iv = cand_idx[src + i];
-        }
-        __syncthreads();
-        if (i < cnt) {
-          cand_key[dst + i] = kv;
-          cand_idx[dst + i] = iv;
-        }
-        __syncthreads();
+    // close the gaps between the warp regions (in warp order = index order):
+    // every thread reads its compacted positions i = tid + j*threads from
+    // their regions into registers, then, after one barrier, writes them
+    int pre[kTopkWarps];
+    {
+      int acc = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) {
+        pre[w] = acc;
+        acc += warp_cnt[w];
       }
-      dst += cnt;
     }
+    constexpr int J = kCandCap / kTopkThreads;
+    uint32_t kv[J];
+    int32_t iv[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int i = threadIdx.x + j * kTopkThreads;
+      kv[j] = 0u;
+      iv[j] = 0;
+      if (j * kTopkThreads >= m) break;   // block-uniform
+      if (i < m) {
+        int src = i;
+#pragma unroll
+        for (int w = 1; w < kTopkWarps; ++w)
+          if (i >= pre[w]) src = i - pre[w] + w * kWarpCap;
+        kv[j] = cand_key[src];
+        iv[j] = cand_idx[src];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int i = threadIdx.x + j * kTopkThreads;
+      if (j * kTopkThreads >= m) break;   // block-uniform
+      if (i < m) {
+        cand_key[i] = kv[j];
+        cand_idx[i] = iv[j];
+      }
+    }
+    __syncthreads();
     select_from_candidates(cand_key, cand_idx, m, k, hist, warp_buf, sel, out);
     return;
   }
