@@ -322,15 +322,26 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         }
         __syncwarp();
         float* gdst = which ? dK : dV;
+        // per pool slot: visible rows and the first row's address (pool 0 for
+        // an empty slot keeps the address valid; its rows are never added)
+        int nrow[4];
+        float* sdst[4];
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int pool = s4 == 0 ? pc[0] : s4 == 1 ? pc[1] : s4 == 2 ? pc[2] : pc[3];
+          nrow[s4] = slot_rows(pool, grp * 4 + s4, k, t);
+          sdst[s4] = gdst + 4 * (int64_t)(pool < 0 ? 0 : pool) * D;
+        }
 #pragma unroll
         for (int kk0 = 0; kk0 < 16; kk0 += ROWS_PER_RED) {
           const int kk = kk0 + lane / RCH;                    // the row this lane adds
           const int lc = lane % RCH;
           const int sig = kk >> 2, row = kk & 3;
-          const int pool = sig == 0 ? pc[0] : sig == 1 ? pc[1] : sig == 2 ? pc[2] : pc[3];
-          const bool ok = row < slot_rows(pool, grp * 4 + sig, k, t);
           const float4 v = ld_shared_v4(tile + kk * RBYTES + ((lc ^ (2 * (kk & 7))) << 4));
-          if (ok) red_add_v4(gdst + (4 * (int64_t)pool + row) * D + lc * 4, v);
+          // predicated, not branched around
+          const int nr = sig == 0 ? nrow[0] : sig == 1 ? nrow[1] : sig == 2 ? nrow[2] : nrow[3];
+          float* dst = sig == 0 ? sdst[0] : sig == 1 ? sdst[1] : sig == 2 ? sdst[2] : sdst[3];
+          red_add_v4_if(dst + row * D + lc * 4, v, row < nr);
         }
         __syncwarp();
       }

@@ -286,6 +286,15 @@ __device__ __forceinline__ void red_add_v4(float* addr, const float4& v) {
                "f"(v.w)
                : "memory");
 }
+// red.global.add.v4.f32 predicated on `pred` (no branch around it).
+__device__ __forceinline__ void red_add_v4_if(float* addr, const float4& v, bool pred) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %5, 0;\n"
+      "@p red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n}\n" ::"l"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((uint32_t)pred)
+      : "memory");
+}
 __device__ __forceinline__ void st_shared_v2(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }

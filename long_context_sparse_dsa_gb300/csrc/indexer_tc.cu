@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     uint32_t acc_iter = 0;
     bool ok = true;
     float* w_mine = w_s + ew * C::QPW * HI;  // this warp's QPW queries x HI weights
+    const uint32_t w_mine_s = smem_u32(w_mine);
     uint32_t stg_iter = 0;
     constexpr int NLD = C::QPW * HI / 16;    // 16-column TMEM loads per tile
     while (ok && it.next<C::BN, C::BM, C::SEG>()) {
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         for (int j = 0; j < C::QPW; ++j) acc[j] = 0.f;
 #pragma unroll
         for (int c4 = 0; c4 < NLD * 4; ++c4) {
-          const float4 q4 = reinterpret_cast<const float4*>(w_mine)[c4];   // broadcast
+          const float4 q4 = ld_shared_v4(w_mine_s + 16 * c4);   // broadcast (explicit shared load)
           const float wq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {

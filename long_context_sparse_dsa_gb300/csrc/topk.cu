@@ -87,26 +87,45 @@ __device__ __forceinline__ void hist_add(int* hist, int bin) {
 
 // Find, scanning bins from the top, the bin where the running count reaches
 // `need`.  Writes the bin and the count strictly above it to sel[0], sel[1].
-__device__ __forceinline__ void find_bin(const int* hist, int nbins, int need, int* warp_buf, int* sel) {
-  const int per = (nbins + kTopkThreads - 1) / kTopkThreads;
-  int local = 0;
-  for (int j = 0; j < per; ++j) {
-    const int b = nbins - 1 - (threadIdx.x * per + j);
-    if (b >= 0) local += hist[b];
+// NBINS is 1024 or 2048: each thread owns 4 or 8 consecutive bins, read as
+// int4 vectors into registers.
+template <int NBINS>
+__device__ __forceinline__ void find_bin(const int* hist, int need, int* warp_buf, int* sel) {
+  constexpr int PER = NBINS / kTopkThreads;
+  static_assert(PER == 4 || PER == 8, "4 or 8 bins per thread");
+  // thread i owns the bins NBINS-PER*(i+1) .. NBINS-1-PER*i (thread 0 the highest)
+  const int lo = NBINS - PER * (threadIdx.x + 1);
+  int h[PER];
+#pragma unroll
+  for (int v = 0; v < PER / 4; ++v) {
+    const int4 x = reinterpret_cast<const int4*>(hist + lo)[v];
+    h[4 * v] = x.x;
+    h[4 * v + 1] = x.y;
+    h[4 * v + 2] = x.z;
+    h[4 * v + 3] = x.w;
   }
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) local += h[j];
   int total;
   int cum = block_excl_scan(local, warp_buf, &total);
-  for (int j = 0; j < per; ++j) {
-    const int b = nbins - 1 - (threadIdx.x * per + j);
-    if (b < 0) break;
-    const int h = hist[b];
-    if (cum < need && cum + h >= need) {
-      sel[0] = b;
-      sel[1] = cum;
+  if (cum < need && cum + local >= need) {
+#pragma unroll
+    for (int j = PER - 1; j >= 0; --j) {   // from the highest bin down
+      if (cum < need && cum + h[j] >= need) {
+        sel[0] = lo + j;
+        sel[1] = cum;
+      }
+      cum += h[j];
     }
-    cum += h;
   }
   __syncthreads();
+}
+
+// Zero the first NBINS histogram bins (int4 stores).
+template <int NBINS>
+__device__ __forceinline__ void zero_hist(int* hist) {
+  for (int b = threadIdx.x; b < NBINS / 4; b += kTopkThreads) reinterpret_cast<int4*>(hist)[b] = make_int4(0, 0, 0, 0);
 }
 
 // `need`-th largest key among keys[0..m) (need <= m) by radix rounds of
@@ -124,7 +143,10 @@ __device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int 
 #pragma unroll
   for (int round = 0; round < ROUNDS; ++round) {
     const int nb = 1 << widths[round];
-    for (int b = threadIdx.x; b < nb; b += kTopkThreads) hist[b] = 0;
+    if (round < 2)
+      zero_hist<2048>(hist);
+    else
+      zero_hist<1024>(hist);
     __syncthreads();
     const int sh = shifts[round];
     const int hi = sh + widths[round];   // bits above this digit must equal the prefix
@@ -138,7 +160,10 @@ __device__ __forceinline__ uint32_t select_kth(const uint32_t* keys, int m, int 
       hist_add(hist, bin);
     }
     __syncthreads();
-    find_bin(hist, nb, need, warp_buf, sel);
+    if (round < 2)
+      find_bin<2048>(hist, need, warp_buf, sel);
+    else
+      find_bin<1024>(hist, need, warp_buf, sel);
     prefix = (prefix << widths[round]) | (uint32_t)sel[0];
     need -= sel[1];
     got_above += sel[1];
@@ -199,7 +224,7 @@ __device__ __forceinline__ void select_from_candidates(const uint32_t* cand_key,
 __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
                                                             int64_t q_begin, int64_t q_count,
                                                             int32_t* __restrict__ idx) {
-  __shared__ int hist[2048];
+  __shared__ __align__(16) int hist[2048];
   __shared__ int warp_buf[32];
   __shared__ int sel[4];
   __shared__ int warp_cnt[kTopkWarps];
@@ -364,7 +389,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       for (int j = 0; j < 4; ++j) kk[j] = (base + j < n) ? order_key(__ldg(row + base + j)) : 0u;
     }
   };
-  for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
+  zero_hist<2048>(hist);
   __syncthreads();
   for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
     uint32_t kk[4];
@@ -373,7 +398,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
     for (int j = 0; j < 4; ++j) hist_add(hist, base + j < n ? (int)(kk[j] >> 21) : -1);
   }
   __syncthreads();
-  find_bin(hist, 2048, k, warp_buf, sel);
+  find_bin<2048>(hist, k, warp_buf, sel);
   const uint32_t b0 = (uint32_t)sel[0];
   const int n_cand = sel[1] + hist[b0];
   __syncthreads();
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
   }
   // tie-heavy: rounds 1 and 2 over the row, then the ordered selection over the row
   const int need1 = k - sel[1];
-  for (int b = threadIdx.x; b < 2048; b += kTopkThreads) hist[b] = 0;
+  zero_hist<2048>(hist);
   __syncthreads();
   for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
     uint32_t kk[4];
@@ -416,10 +441,10 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       hist_add(hist, (base + j < n && (kk[j] >> 21) == b0) ? (int)((kk[j] >> 10) & 0x7FFu) : -1);
   }
   __syncthreads();
-  find_bin(hist, 2048, need1, warp_buf, sel);
+  find_bin<2048>(hist, need1, warp_buf, sel);
   const uint32_t pre1 = (b0 << 11) | (uint32_t)sel[0];
   const int need2 = need1 - sel[1];
-  for (int b = threadIdx.x; b < 1024; b += kTopkThreads) hist[b] = 0;
+  zero_hist<1024>(hist);
   __syncthreads();
   for (int base = threadIdx.x * 4; base < n_round; base += 4 * kTopkThreads) {
     uint32_t kk[4];
@@ -429,7 +454,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       hist_add(hist, (base + j < n && (kk[j] >> 10) == pre1) ? (int)(kk[j] & 0x3FFu) : -1);
   }
   __syncthreads();
-  find_bin(hist, 1024, need2, warp_buf, sel);
+  find_bin<1024>(hist, need2, warp_buf, sel);
   const uint32_t T = (pre1 << 10) | (uint32_t)sel[0];
   const int need_eq = need2 - sel[1];
   int eq_seen = 0, taken = 0;
