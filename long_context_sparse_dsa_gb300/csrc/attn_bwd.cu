@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   const GatherLane<D> gl = gather_lane<D>(lane);
   const int nsteps = ngroups;
   int pc[4];
-  step_pools(irow, k, 0, t, lane, pc);
+  bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
+  step_pools(irow, k, 0, t, pc, bad_idx);
   gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
   cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       const int nx = step + 1;
       if (nx < nsteps) {
         const int grp_n = nx;
-        step_pools(irow, k, grp_n, t, lane, pf);
+        step_pools(irow, k, grp_n, t, pf, bad_idx);
         gather_step16<D>(wbase + (nx & 1) * C::STAGE_BYTES, K, V, pf, gl, t, k, grp_n);
       }
       cp_async_commit();
@@ -236,14 +237,11 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       // D partial sums over this lane's columns: rows g and g+8
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        if (kv[nt][0]) {
-          Dg = fmaf(ex2_approx(s[nt][0] * scale_log2 - lse_g), dp[nt][0], Dg);
-          Dg8 = fmaf(ex2_approx(s[nt][2] * scale_log2 - lse_g8), dp[nt][2], Dg8);
-        }
-        if (kv[nt][1]) {
-          Dg = fmaf(ex2_approx(s[nt][1] * scale_log2 - lse_g), dp[nt][1], Dg);
-          Dg8 = fmaf(ex2_approx(s[nt][3] * scale_log2 - lse_g8), dp[nt][3], Dg8);
-        }
+        // an invisible key gets P = +0 (its zero-filled V row gives dP = 0)
+        Dg = fmaf(ex2_approx(kv[nt][0] ? s[nt][0] * scale_log2 - lse_g : -INFINITY), dp[nt][0], Dg);
+        Dg8 = fmaf(ex2_approx(kv[nt][0] ? s[nt][2] * scale_log2 - lse_g8 : -INFINITY), dp[nt][2], Dg8);
+        Dg = fmaf(ex2_approx(kv[nt][1] ? s[nt][1] * scale_log2 - lse_g : -INFINITY), dp[nt][1], Dg);
+        Dg8 = fmaf(ex2_approx(kv[nt][1] ? s[nt][3] * scale_log2 - lse_g8 : -INFINITY), dp[nt][3], Dg8);
       }
       __syncwarp();
 #pragma unroll
@@ -254,10 +252,11 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     uint32_t pp[2][2], dd[2][2], dh[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float p0 = kv[nt][0] ? ex2_approx(s[nt][0] * scale_log2 - lse_g) : 0.f;
-      const float p1 = kv[nt][1] ? ex2_approx(s[nt][1] * scale_log2 - lse_g) : 0.f;
-      const float p2 = kv[nt][0] ? ex2_approx(s[nt][2] * scale_log2 - lse_g8) : 0.f;
-      const float p3 = kv[nt][1] ? ex2_approx(s[nt][3] * scale_log2 - lse_g8) : 0.f;
+      // an invisible key gets 2^-inf = +0 exactly (no branch around the ex2)
+      const float p0 = ex2_approx(kv[nt][0] ? s[nt][0] * scale_log2 - lse_g : -INFINITY);
+      const float p1 = ex2_approx(kv[nt][1] ? s[nt][1] * scale_log2 - lse_g : -INFINITY);
+      const float p2 = ex2_approx(kv[nt][0] ? s[nt][2] * scale_log2 - lse_g8 : -INFINITY);
+      const float p3 = ex2_approx(kv[nt][1] ? s[nt][3] * scale_log2 - lse_g8 : -INFINITY);
       const float s0 = scale * p0 * (dp[nt][0] - Dg), s1 = scale * p1 * (dp[nt][1] - Dg);
       const float s2 = scale * p2 * (dp[nt][2] - Dg8), s3 = scale * p3 * (dp[nt][3] - Dg8);
       pp[nt][0] = pack_f16(p0, p1);
@@ -351,6 +350,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
   }
   cp_async_wait<0>();
+  if (bad_idx && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
   if (PASS == 1) {
     Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
     Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);

@@ -90,12 +90,13 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
 
   // pools of the current step (pc) and, with three stages, of the next (pn)
   int pc[4], pn[4] = {-1, -1, -1, -1};
-  step_pools(irow, k, 0, t, lane, pc);
+  bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
+  step_pools(irow, k, 0, t, pc, bad_idx);
   gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
   cp_async_commit();
   if constexpr (NST == 3) {
     if (ngroups > 1) {
-      step_pools(irow, k, 1, t, lane, pn);
+      step_pools(irow, k, 1, t, pn, bad_idx);
       gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl, t, k, 1);
     }
     cp_async_commit();
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     {
       const int nx = grp + NST - 1;
       if (nx < ngroups) {
-        step_pools(irow, k, nx, t, lane, pf);
+        step_pools(irow, k, nx, t, pf, bad_idx);
         const int st = stage + NST - 1 >= NST ? stage - 1 : stage + NST - 1;
         gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl, t, k, nx);
       }
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     stage = stage == NST - 1 ? 0 : stage + 1;
   }
   cp_async_wait<0>();
+  if (bad_idx && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
 
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);

@@ -7,8 +7,8 @@
 // position c ^ (r & 7), which makes the ldmatrix reads conflict-free.
 //
 // Everything that depends only on the lane is computed once (GatherLane);
-// per step a lane needs the 4 pool indices of the step (one 32-bit shuffle
-// each), one address per pool slot, and then one compare per copy.  Keys that
+// per step a lane needs the 4 pool indices of the step (broadcast loads),
+// one address per pool slot, and then one compare per copy.  Keys that
 // are not visible (empty slot, or tokens after t in the partial pool) are
 // zero-filled.
 #pragma once
@@ -60,35 +60,33 @@ __device__ __forceinline__ GatherLane<D> gather_lane(int lane) {
   return g;
 }
 
-// Pool of slot `slot` for query t (slot k = the own partial pool), -1 if none.
-// A pool the query may not see is recorded as a bad index and skipped.
-__device__ __forceinline__ int slot_pool32(const int32_t* irow, int k, int slot, int64_t t) {
-  if (slot < k) {
-    const int p = __ldg(irow + slot);
-    if (p < 0) return -1;
-    if ((int64_t)p >= elig(t)) {
-      record_error(DSA_DEV_ERR_BAD_INDEX);
-      return -1;
-    }
-    return p;
-  }
-  if (slot == k && (t & 3) != 3) return (int)(t >> 2);
-  return -1;
-}
-
-// The 4 pools of step `grp` for every lane (lanes 0..3 read idx, then shuffle).
-__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, int lane, int (&pools)[4]) {
-  const int mine = lane < 4 ? slot_pool32(irow, k, grp * 4 + lane, t) : -1;
+// The 4 pools of step `grp` (slots grp*4 .. grp*4+3; slot k is the own partial
+// pool, -1 when there is none).  Every lane reads the 4 idx entries itself
+// (the same addresses across the warp: broadcast loads) and decides with
+// selects, so no lane-divergent branch is taken.  An entry outside the causal
+// range is skipped (-1) and sets `bad`, which the caller reports once.
+__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, int (&pools)[4],
+                                           bool& bad) {
+  const int el = (int)elig(t);
+  const int part = (t & 3) != 3 ? (int)(t >> 2) : -1;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) pools[s] = __shfl_sync(0xffffffffu, mine, s);
+  for (int s = 0; s < 4; ++s) {
+    const int slot = grp * 4 + s;
+    const bool sel = slot < k;
+    const int raw = __ldg(irow + (sel ? slot : 0));   // a valid address either way (k >= 1)
+    const bool out = sel && raw >= el;
+    bad |= out;
+    pools[s] = sel ? ((raw < 0 || out) ? -1 : raw) : (slot == k ? part : -1);
+  }
 }
 
 // Number of visible tokens of slot s (4 for a selected pool, 1..3 for the
-// partial pool, 0 for an empty slot).
+// partial pool, 0 for an empty slot).  `pool` is what step_pools gave for
+// the slot, so the partial pool (slot k) is t/4 and holds tokens 4*(t/4)..t.
 __device__ __forceinline__ int slot_rows(int pool, int slot, int k, int64_t t) {
   if (pool < 0) return 0;
   if (slot != k) return 4;
-  return (int)(t - 4 * (int64_t)pool) + 1;
+  return (int)(t & 3) + 1;
 }
 
 template <int D>
