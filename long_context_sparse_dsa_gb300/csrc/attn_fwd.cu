@@ -15,8 +15,8 @@
 // tile (2-stage ring per warp, no CTA-wide barriers).  The 16 heads of one
 // query share every gathered key, which makes heads the M=16 side of
 // m16n8k16 bf16 MMAs: S = Q K^T and O += P V, fp32 accumulation, online
-// softmax in registers.  The kernel is bound by the L2->SM gather bandwidth
-// (about 16 flop per gathered byte), not by the MMAs.
+// softmax in registers with a lazily moved base.  The kernel is bound by the
+// L2->SM gather and by issue (about 16 flop per gathered byte), not by the MMAs.
 //
 // With an o_acc buffer (the ACC variant) the probabilities enter P V as two
 // bf16 terms, P = hi + lo with hi = bf16(P) and lo = bf16(P - hi), so the fp32
@@ -44,6 +44,8 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   hi = pack_bf16(x0, x1);
   lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
 }
+
+constexpr float kLazyLog2 = 8.f;   // the softmax base lags the running max by at most this (log2 units)
 
 template <int D, int NST, int MINB, bool ACC>
 __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfloat16* __restrict__ Q,
@@ -172,9 +174,13 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    // Lazy rescaling: the exponent base m moves only when the step's max
+    // exceeds it by more than kLazyLog2 (so P <= 2^kLazyLog2 in fp32, and
+    // O and l are rescaled rarely); LSE = m + log2(l) holds for any base.
+    const bool up0 = mx0 > m0 + kLazyLog2, up1 = mx1 > m1 + kLazyLog2;
+    const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
     const float base0 = mn0 == -INFINITY ? 0.f : mn0, base1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = ex2_approx(m0 - base0), a1 = ex2_approx(m1 - base1);
+    const float a0 = up0 ? ex2_approx(m0 - base0) : 1.f, a1 = up1 ? ex2_approx(m1 - base1) : 1.f;
     m0 = mn0;
     m1 = mn1;
     float rs0 = 0.f, rs1 = 0.f;

@@ -69,6 +69,30 @@ struct IdxCfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
+// One-lane operations of the epilogue as predicated instructions (no branch
+// and no reconvergence around them): the lane with `pred` set performs them.
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n@p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(bar),
+               "r"((uint32_t)pred)
+               : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_if(bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %1, 0;\n@p cp.async.bulk.wait_group.read %0;\n}\n" ::"n"(N),
+               "r"((uint32_t)pred)
+               : "memory");
+}
+// TMA tile store of `src` at (x, y), then commit of the bulk group.
+__device__ __forceinline__ void tma_store_2d_commit_if(const void* tmap, uint32_t src, int32_t x, int32_t y,
+                                                       bool pred) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "@p cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];\n"
+      "@p cp.async.bulk.commit_group;\n}\n" ::"l"(tmap),
+      "r"(src), "r"(x), "r"(y), "r"((uint32_t)pred)
+      : "memory");
+}
+
 struct UnitIter {
   int64_t q_begin, q_end, nqb, maxseg, P;
   int64_t u, stride;
@@ -266,7 +290,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         // the accumulator is in registers: hand it back to the MMA warp
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(ab));
+        mbar_arrive_if(tempty(ab), lane == 0);
         float acc[C::QPW];
 #pragma unroll
         for (int j = 0; j < C::QPW; ++j) acc[j] = 0.f;
@@ -287,18 +311,15 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
           // written too (the top-k never reads them)
           const int sb = stg_iter % C::NSTG;
           const uint32_t stg = smem_u32(smem + C::OFF_STG) + (ew * C::NSTG + sb) * C::STG_BYTES;
-          if (lane == 0 && stg_iter >= C::NSTG) bulk_wait_read<C::NSTG - 1>();
+          bulk_wait_read_if<C::NSTG - 1>(lane == 0 && stg_iter >= C::NSTG);
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < C::QPW; ++j)
             asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(stg + (j * 32 + lane) * 4), "f"(acc[j]) : "memory");
           fence_proxy_async_shared();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmap_s, stg, (int32_t)(tile * C::BM + lane_base),
-                         (int32_t)(it.t0 - q_begin + qg * C::QPW));
-            bulk_commit();
-          }
+          tma_store_2d_commit_if(&tmap_s, stg, (int32_t)(tile * C::BM + lane_base),
+                                 (int32_t)(it.t0 - q_begin + qg * C::QPW), lane == 0);
           ++stg_iter;
         } else {
 #pragma unroll

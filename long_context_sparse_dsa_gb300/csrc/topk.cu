@@ -78,11 +78,31 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_buf, int* total)
   return base + incl - v;
 }
 
-// Histogram add with warp aggregation (many equal keys in tie-heavy rows).
+// Predicated shared-memory writes: one instruction each, no branch around
+// them (a predicated-off instruction does not touch its address).
+__device__ __forceinline__ void st_shared_u32_if(uint32_t addr, uint32_t v, bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n@p st.shared.u32 [%0], %1;\n}\n" ::"r"(addr), "r"(v),
+               "r"((uint32_t)pred)
+               : "memory");
+}
+__device__ __forceinline__ void red_shared_add_if(uint32_t addr, uint32_t v, bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n@p red.shared.add.u32 [%0], %1;\n}\n" ::"r"(addr),
+               "r"(v), "r"((uint32_t)pred)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_s32_if(int32_t* addr, int32_t v, bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n@p st.global.s32 [%0], %1;\n}\n" ::"l"(addr), "r"(v),
+               "r"((uint32_t)pred)
+               : "memory");
+}
+
+// Histogram add with warp aggregation (many equal keys in tie-heavy rows):
+// the lowest lane of each group of equal bins adds the group's size.
 __device__ __forceinline__ void hist_add(int* hist, int bin) {
   const unsigned peers = __match_any_sync(0xffffffffu, bin);
   const int leader = __ffs(peers) - 1;
-  if ((int)(threadIdx.x & 31) == leader && bin >= 0) atomicAdd(&hist[bin], __popc(peers));
+  red_shared_add_if(smem_u32(hist) + 4u * (uint32_t)bin, (uint32_t)__popc(peers),
+                    (int)(threadIdx.x & 31) == leader && bin >= 0);
 }
 
 // Find, scanning bins from the top, the bin where the running count reaches
@@ -198,8 +218,12 @@ __device__ __forceinline__ void select_tile(const uint32_t (&kk)[4], int base, i
   int take_total;
   int pos = taken + block_excl_scan(n_take, warp_buf, &take_total);
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (take[j]) out[pos++] = ids ? ids[base + j] : base + j;
+  for (int j = 0; j < 4; ++j) {
+    // ids[] is read for every valid position (taken or not) so the store can be predicated
+    const int32_t v = ids ? (base + j < n ? ids[base + j] : 0) : base + j;
+    st_global_s32_if(out + pos, v, take[j]);
+    pos += take[j];
+  }
   eq_seen += eq_total;
   taken += take_total;
 }
@@ -271,8 +295,8 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
   const int w_end = min(n, w_begin + seg);
   int wcount = 0;
   bool overflow = false;
-  uint32_t* my_key = cand_key + wid * kWarpCap;
-  int32_t* my_idx = cand_idx + wid * kWarpCap;
+  const uint32_t my_key_s = smem_u32(cand_key + wid * kWarpCap);
+  const uint32_t my_idx_s = smem_u32(cand_idx + wid * kWarpCap);
   for (int base = w_begin; base < w_end && !overflow; base += 128 * kStreamUnroll) {
     uint32_t kk[kStreamUnroll][4];
 #pragma unroll
@@ -312,12 +336,11 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       }
       int pos = wcount + incl - c;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (f[j]) {
-          my_key[pos] = kk[u][j];
-          my_idx[pos] = e + j;
-          ++pos;
-        }
+      for (int j = 0; j < 4; ++j) {
+        st_shared_u32_if(my_key_s + 4u * pos, kk[u][j], f[j]);
+        st_shared_u32_if(my_idx_s + 4u * pos, (uint32_t)(e + j), f[j]);
+        pos += f[j];
+      }
       wcount += tot;
     }
   }
@@ -342,35 +365,40 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
         acc += warp_cnt[w];
       }
     }
-    constexpr int J = kCandCap / kTopkThreads;
-    uint32_t kv[J];
-    int32_t iv[J];
+    // in passes of J*threads positions; a candidate's source position is
+    // never below its destination, so a later pass reads nothing an earlier
+    // pass wrote
+    constexpr int J = 8;
+    for (int pass0 = 0; pass0 < m; pass0 += J * kTopkThreads) {
+      uint32_t kv[J];
+      int32_t iv[J];
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int i = threadIdx.x + j * kTopkThreads;
-      kv[j] = 0u;
-      iv[j] = 0;
-      if (j * kTopkThreads >= m) break;   // block-uniform
-      if (i < m) {
-        int src = i;
+      for (int j = 0; j < J; ++j) {
+        const int i = pass0 + threadIdx.x + j * kTopkThreads;
+        kv[j] = 0u;
+        iv[j] = 0;
+        if (pass0 + j * kTopkThreads >= m) break;   // block-uniform
+        if (i < m) {
+          int src = i;
 #pragma unroll
-        for (int w = 1; w < kTopkWarps; ++w)
-          if (i >= pre[w]) src = i - pre[w] + w * kWarpCap;
-        kv[j] = cand_key[src];
-        iv[j] = cand_idx[src];
+          for (int w = 1; w < kTopkWarps; ++w)
+            if (i >= pre[w]) src = i - pre[w] + w * kWarpCap;
+          kv[j] = cand_key[src];
+          iv[j] = cand_idx[src];
+        }
       }
-    }
-    __syncthreads();
+      __syncthreads();
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int i = threadIdx.x + j * kTopkThreads;
-      if (j * kTopkThreads >= m) break;   // block-uniform
-      if (i < m) {
-        cand_key[i] = kv[j];
-        cand_idx[i] = iv[j];
+      for (int j = 0; j < J; ++j) {
+        const int i = pass0 + threadIdx.x + j * kTopkThreads;
+        if (pass0 + j * kTopkThreads >= m) break;   // block-uniform
+        if (i < m) {
+          cand_key[i] = kv[j];
+          cand_idx[i] = iv[j];
+        }
       }
+      __syncthreads();
     }
-    __syncthreads();
     select_from_candidates(cand_key, cand_idx, m, k, hist, warp_buf, sel, out);
     return;
   }
@@ -417,12 +445,11 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       int tot;
       int pos = written + block_excl_scan(cnt, warp_buf, &tot);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (f[j]) {
-          cand_key[pos] = kk[j];
-          cand_idx[pos] = base + j;
-          ++pos;
-        }
+      for (int j = 0; j < 4; ++j) {
+        st_shared_u32_if(smem_u32(cand_key) + 4u * pos, kk[j], f[j]);
+        st_shared_u32_if(smem_u32(cand_idx) + 4u * pos, (uint32_t)(base + j), f[j]);
+        pos += f[j];
+      }
       written += tot;
     }
     __syncthreads();
