@@ -24,10 +24,12 @@
 // from a per-warp swizzled shared copy.  The dK/dV products run in fp16
 // (P, scale*dS, Q, dO converted; 10-bit mantissa instead of bf16's 7) because
 // those sums collect contributions from every query that selected a key.
-// Each finished 16-key dK/dV tile is staged in shared memory and added to
-// global memory one key row per warp instruction (red.global.add.v4.f32 over
-// a contiguous 512-byte row), which the L2 absorbs about 1.6x faster than
-// fragment-shaped reductions; the summation order across queries is not fixed.
+// Each finished 16-key dK/dV tile is staged in shared memory (rows padded so
+// the fragment writes do not conflict) and each visible key row is added to
+// global memory by one bulk fp32 reduction of the TMA engine
+// (cp.reduce.async.bulk, one contiguous row of D floats).  Row-contiguous
+// reductions are absorbed by the L2 about 1.6x faster than fragment-shaped
+// ones; the summation order across queries is not fixed.
 #include "common.cuh"
 #include "gather.cuh"
 #include "launch.h"
@@ -42,11 +44,36 @@ struct BwdCfg {
   static constexpr int CHUNKS = GatherCfg<D>::CHUNKS;
   static constexpr int TILE_BYTES = GatherCfg<D>::TILE_BYTES;
   static constexpr int STAGE_BYTES = GatherCfg<D>::STAGE_BYTES;
+  // A consumed stage also holds a 16-key fp32 dK or dV tile with rows RED_PITCH
+  // bytes apart (a row of D fp32 plus 32 bytes, which keeps the fragment
+  // writes free of bank conflicts), so each stage is followed by padding.
+  static constexpr int RED_ROW = D * 4;
+  static constexpr int RED_PITCH = RED_ROW + 32;
+  static constexpr int STAGE_PITCH = 16 * RED_PITCH > STAGE_BYTES ? 16 * RED_PITCH : STAGE_BYTES;
   static constexpr int NST = 2;
   static constexpr int WARPS = 4;
-  static constexpr int WARP_BYTES = NST * STAGE_BYTES + (PASS == 2 ? 2 * TILE_BYTES : 0);
+  static constexpr int WARP_BYTES = NST * STAGE_PITCH + (PASS == 2 ? 2 * TILE_BYTES : 0);
   static constexpr int SMEM = WARPS * WARP_BYTES;
+  static_assert(STAGE_PITCH % 16 == 0 && WARP_BYTES % 16 == 0 && RED_PITCH % 16 == 0, "16-byte alignment");
 };
+
+// Bulk (TMA-engine) fp32 add of `bytes` contiguous shared-memory bytes into
+// global memory, then a commit of this thread's bulk group; both only where
+// `pred` holds.
+__device__ __forceinline__ void bulk_red_add_f32_if(float* gdst, uint32_t ssrc, uint32_t bytes, bool pred) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %3, 0;\n"
+      "@p cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n"
+      "@p cp.async.bulk.commit_group;\n}\n" ::"l"(gdst),
+      "r"(ssrc), "r"(bytes), "r"((uint32_t)pred)
+      : "memory");
+}
+// Wait (where `pred` holds) until this thread's bulk groups no longer read shared memory.
+__device__ __forceinline__ void bulk_wait_read0_if(bool pred) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %0, 0;\n@p cp.async.bulk.wait_group.read 0;\n}\n" ::"r"(
+                   (uint32_t)pred)
+               : "memory");
+}
 
 // Eight bf16 values -> eight fp16 values (exact for |x| in [2^-14, 65504]).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
@@ -74,7 +101,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   const int64_t t = item / HG;
   const int hg = (int)(item % HG);
   const uint32_t wbase = smem_u32(bwd_smem) + warp * C::WARP_BYTES;
-  const uint32_t qs = wbase + C::NST * C::STAGE_BYTES;
+  const uint32_t qs = wbase + C::NST * C::STAGE_PITCH;
   const uint32_t dos = qs + C::TILE_BYTES;
   const int32_t* irow = idx + t * k;
   const int nslots = k + 1;
@@ -175,9 +202,15 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     {
       const int nx = step + 1;
       if (nx < nsteps) {
+        // the stage being refilled held the previous step's dK tile: its bulk
+        // reductions must have finished reading it
+        if (PASS == 2) {
+          bulk_wait_read0_if(lane < 16);
+          __syncwarp();
+        }
         const int grp_n = nx;
         step_pools(irow, k, grp_n, t, pf, bad_idx);
-        gather_step16<D>(wbase + (nx & 1) * C::STAGE_BYTES, K, V, pf, gl, t, k, grp_n);
+        gather_step16<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl, t, k, grp_n);
       }
       cp_async_commit();
     }
@@ -193,7 +226,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
-    const uint32_t ks_base = wbase + stage * C::STAGE_BYTES;
+    const uint32_t ks_base = wbase + stage * C::STAGE_PITCH;
     const uint32_t vs_base = ks_base + C::TILE_BYTES;
 
     // S = Q K^T and dP = dO V^T (heads x 16 keys), each as two independent
@@ -285,24 +318,32 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const uint32_t dt0 = movmatrix_t(dh[0][0]), dt1 = movmatrix_t(dh[1][0]);
     const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
     // The step's K/V stage is free now (S, dP and dQ are done).  Each 16-key
-    // fp32 tile (dV, then dK) is written into it, 16-byte chunk c of row r at
-    // position c ^ 2(r & 7): a half-warp's fragment writes (rows g..g+3, two
-    // adjacent chunks each) then hit distinct bank groups, and a row read is a
-    // permutation of the row.  It is then added to global memory one key row
-    // at a time: the whole warp covers a row with one contiguous reduction.
+    // fp32 tile (dV, then dK) is written into it in fragment order, row r at
+    // r * RED_PITCH: the 32-byte row padding puts the 8 rows of one fragment
+    // write in distinct bank groups.  Then lanes 0..15 each hand one visible
+    // key row (D fp32, contiguous) to the TMA engine as one bulk fp32
+    // reduction into global memory.
     __syncwarp();
     {
-      constexpr int RCH = D / 4;              // 16-byte chunks per fp32 row
-      constexpr int RBYTES = D * 4;
-      constexpr int ROWS_PER_RED = 32 / RCH;  // rows covered by one warp instruction
       const int mtx = lane >> 3, r = lane & 7;
       const int hrow = (mtx & 1) * 8 + r;
       const uint32_t tile = ks_base;
+      const uint32_t frag = tile + g * C::RED_PITCH + 8 * qi;   // this lane's (row g, columns 2qi..) slot
+      // the row this lane reduces (lanes 0..15): key lane of the step
+      const int rsig = (lane >> 2) & 3, rrow = lane & 3;
+      const int rpool = rsig == 0 ? pc[0] : rsig == 1 ? pc[1] : rsig == 2 ? pc[2] : pc[3];
+      const bool rok = lane < 16 && rrow < slot_rows(rpool, grp * 4 + rsig, k, t);
+      const int64_t rrow_g = 4 * (int64_t)(rpool < 0 ? 0 : rpool) + rrow;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV = P^T dO, 1: dK = (scale dS)^T Q
         const uint32_t bsrc = which ? qs : dos;
         const uint32_t a0 = which ? dt0 : pt0, a1 = which ? dt1 : pt1;
         const uint32_t a2 = which ? dt2 : pt2, a3 = which ? dt3 : pt3;
+        if (which == 1) {
+          // the dV tile's reductions must have read it before dK overwrites it
+          bulk_wait_read0_if(lane < 16);
+          __syncwarp();
+        }
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
           const int ch = 2 * j + (mtx >> 1);
@@ -313,36 +354,15 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
           mma_f16_16816(c2[1], a0, a1, a2, a3, b2, b3);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int c = (2 * j + h) * 2 + (qi >> 1);          // fp32 chunk of columns (2j+h)*8 + 2qi
-            const uint32_t off = (uint32_t)(((c ^ (2 * (g & 7))) << 4) + (qi & 1) * 8);
-            st_shared_v2(tile + g * RBYTES + off, c2[h][0], c2[h][1]);
-            st_shared_v2(tile + (g + 8) * RBYTES + off, c2[h][2], c2[h][3]);
+            const uint32_t off = (uint32_t)((2 * j + h) * 32);   // columns (2j+h)*8 + 2qi, +1
+            st_shared_v2(frag + off, c2[h][0], c2[h][1]);
+            st_shared_v2(frag + 8 * C::RED_PITCH + off, c2[h][2], c2[h][3]);
           }
         }
+        fence_proxy_async_shared();   // the tile's generic-proxy writes before the bulk reads
         __syncwarp();
         float* gdst = which ? dK : dV;
-        // per pool slot: visible rows and the first row's address (pool 0 for
-        // an empty slot keeps the address valid; its rows are never added)
-        int nrow[4];
-        float* sdst[4];
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int pool = s4 == 0 ? pc[0] : s4 == 1 ? pc[1] : s4 == 2 ? pc[2] : pc[3];
-          nrow[s4] = slot_rows(pool, grp * 4 + s4, k, t);
-          sdst[s4] = gdst + 4 * (int64_t)(pool < 0 ? 0 : pool) * D;
-        }
-#pragma unroll
-        for (int kk0 = 0; kk0 < 16; kk0 += ROWS_PER_RED) {
-          const int kk = kk0 + lane / RCH;                    // the row this lane adds
-          const int lc = lane % RCH;
-          const int sig = kk >> 2, row = kk & 3;
-          const float4 v = ld_shared_v4(tile + kk * RBYTES + ((lc ^ (2 * (kk & 7))) << 4));
-          // predicated, not branched around
-          const int nr = sig == 0 ? nrow[0] : sig == 1 ? nrow[1] : sig == 2 ? nrow[2] : nrow[3];
-          float* dst = sig == 0 ? sdst[0] : sig == 1 ? sdst[1] : sig == 2 ? sdst[2] : sdst[3];
-          red_add_v4_if(dst + row * D + lc * 4, v, row < nr);
-        }
-        __syncwarp();
+        bulk_red_add_f32_if(gdst + rrow_g * D, tile + (lane & 15) * C::RED_PITCH, (uint32_t)C::RED_ROW, rok);
       }
     }
     __syncwarp();
@@ -350,6 +370,9 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
   }
   cp_async_wait<0>();
+  if (PASS == 2) {
+    bulk_wait<0>();   // every bulk reduction of this thread has completed before the CTA exits
+  }
   if (bad_idx && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
   if (PASS == 1) {
     Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
