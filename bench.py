@@ -26,6 +26,7 @@ import argparse
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -59,11 +60,11 @@ def load_peaks():
 # only while the kernel's source files hash as they did when it was captured;
 # after any change to them the bench reports null until it is captured again.
 TRAFFIC = {
-    ("bf16_128k_needle", "attn_bwd"): {"bytes": 11216055296 + 8548524032,
-                                       "sources": {"attn_bwd.cu": "b9177224fe011174", "gather.cuh": "faf57e0a5ee7cd39",
+    ("bf16_128k_needle", "attn_bwd"): {"bytes": 10889421312 + 8083173888,
+                                       "sources": {"attn_bwd.cu": "8e7a7d8c19de40a7", "gather.cuh": "faf57e0a5ee7cd39",
                                                    "common.cuh": "6fbc65a01c30f2d5"}},
-    ("bf16_128k_needle", "attn_fwd"): {"bytes": 1322506496 + 1578370048,
-                                       "sources": {"attn_fwd.cu": "5477076dde6b8a6b", "gather.cuh": "faf57e0a5ee7cd39",
+    ("bf16_128k_needle", "attn_fwd"): {"bytes": 1324816384 + 1578614016,
+                                       "sources": {"attn_fwd.cu": "6bb12523dfda2551", "gather.cuh": "faf57e0a5ee7cd39",
                                                    "common.cuh": "6fbc65a01c30f2d5"}},
 }
 
@@ -198,7 +199,9 @@ def run_ours(args, rank, world):
     dsa.library()
 
     names = ("Q", "K", "V", "q_I", "k_I", "w") + (("dO",) if with_bwd else ())
+    torch.cuda.reset_peak_memory_stats(dev)
     host = dsa_inputs.make(wl, names, pin=True)
+    inputs_sha = inputs_digest(host, names)
     d_in = {n: host[n].to(dev, non_blocking=True) for n in names}
     dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
     # with a backward, the forward keeps its fp32 output for it (the backward
@@ -287,6 +290,14 @@ def run_ours(args, rank, world):
     kernels = {nm: {"ms_per_step": round(k_ms[nm], 4), "launches_per_step": len(per_kernel[nm]) // steps,
                     **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))} for nm in k_ms}
 
+    # device memory of the layer: every buffer is a torch allocation (the library allocates nothing)
+    flush_bytes = flush.numel()
+    peak = torch.cuda.max_memory_allocated(dev)
+    memory = {"peak_allocated_gib": round((peak - flush_bytes) / 2**30, 3),
+              "score_workspace_gib": round(bufs.ws.numel() / 2**30, 3),
+              "what": "torch.cuda.max_memory_allocated over inputs, outputs and workspaces, less the 256 MiB "
+                      "L2-flush buffer; the library allocates no device memory"}
+
     # end-to-end through the C ABI with host buffers: H2D of the inputs, the layer, D2H of the results
     e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev)
     clocks = clk.summary()
@@ -304,6 +315,8 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "memory": memory,
+        "inputs_sha256": inputs_sha,
     }
 
 
@@ -328,6 +341,11 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks):
 
 
 def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev):
+    """Tokens/s through the public entry points with host buffers: every step
+    copies its inputs in from pinned host memory, runs the layer and copies its
+    outputs (O, LSE and, with a backward, dQ, dK, dV) back, all on one stream.
+    Overlapping the copies with the layer (double-buffered, over three
+    streams) and splitting them over four streams both measured slower."""
     names = list(d_in.keys())
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
@@ -359,7 +377,33 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 
-# ---------------------------------------------------------------- oracle
+def inputs_digest(host: dict, names) -> str:
+    """SHA-256 over the host input arrays, in the given tensor order."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        t = host[n].contiguous()
+        h.update(n.encode())
+        h.update(t.view(torch.uint8).numpy().tobytes() if t.dtype != torch.bfloat16
+                 else t.view(torch.int16).numpy().tobytes())
+    return h.hexdigest()
+
+
+def host_cpu() -> dict:
+    """The host's logical CPU count and a model string (best effort)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cpus": os.cpu_count(), "cpu_model": model}
+
+
 def oracle_sample(wl, n_rows: int, seed: int = 7):
     """Time the CPU oracle (single thread) on n_rows query rows of the workload:
     pool keys, the rows' indexer scores and top-k, their attention forward and
@@ -412,7 +456,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "L": wl.L, "k": wl.k, "pass": wl.passes},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, **host_cpu()},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
@@ -444,7 +488,7 @@ def main():
             wl = dsa_inputs.WORKLOADS[args.workload]
             secs, n, desc = oracle_sample(wl, args.cpu_rows)
             line["cpu_baseline"] = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                    "sample": desc, "seconds": round(secs, 2)}
+                                    "sample": desc, "seconds": round(secs, 2), **host_cpu()}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

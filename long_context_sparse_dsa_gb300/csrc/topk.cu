@@ -11,7 +11,9 @@
 // two tie), and an ordered selection keeps every score above that threshold
 // plus the lowest-indexed ties at it.  The output is in ascending pool order
 // and padded with -1; the result depends only on the scores (no atomics
-// decide order), so it is bitwise reproducible.
+// decide order), so it is bitwise reproducible.  Scores are taken to be
+// finite (the indexer gives finite scores for finite inputs): a NaN score has
+// no defined rank.
 //
 // One CTA of kTopkThreads threads per row, one read of the row in the
 // common case:
@@ -48,6 +50,10 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
   if (u == 0x80000000u) u = 0u;  // -0 ties with +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The float whose order key is `key` (key must be the key of a finite value).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Exclusive block-wide scan of one int per thread.  Returns the exclusive
@@ -297,20 +303,26 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
   bool overflow = false;
   const uint32_t my_key_s = smem_u32(cand_key + wid * kWarpCap);
   const uint32_t my_idx_s = smem_u32(cand_idx + wid * kWarpCap);
+  // For a finite score x, order_key(x) >= tau exactly when x >= key_value(tau)
+  // (also for -0 and +0), so the pass compares the floats themselves and keeps
+  // their raw bits; the keys are formed for the candidates only, when the
+  // warp regions are merged.  tau == 0 (no sampling) keeps every score.
+  const bool keep_all = tau == 0u;
+  const float tau_f = keep_all ? 0.f : key_value(tau);
   for (int base = w_begin; base < w_end && !overflow; base += 128 * kStreamUnroll) {
-    uint32_t kk[kStreamUnroll][4];
+    float xx[kStreamUnroll][4];
 #pragma unroll
     for (int u = 0; u < kStreamUnroll; ++u) {
       const int e = base + u * 128 + 4 * lane;
       if (vec4 && e + 3 < w_end) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(row + e));
-        kk[u][0] = order_key(f.x);
-        kk[u][1] = order_key(f.y);
-        kk[u][2] = order_key(f.z);
-        kk[u][3] = order_key(f.w);
+        xx[u][0] = f.x;
+        xx[u][1] = f.y;
+        xx[u][2] = f.z;
+        xx[u][3] = f.w;
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) kk[u][j] = (e + j < w_end) ? order_key(__ldg(row + e + j)) : 0u;
+        for (int j = 0; j < 4; ++j) xx[u][j] = (e + j < w_end) ? __ldg(row + e + j) : 0.f;
       }
     }
 #pragma unroll
@@ -320,7 +332,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       int c = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        f[j] = (e + j < w_end) && kk[u][j] >= tau;
+        f[j] = (e + j < w_end) && (keep_all || xx[u][j] >= tau_f);
         c += f[j];
       }
       int incl = c;
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
       int pos = wcount + incl - c;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        st_shared_u32_if(my_key_s + 4u * pos, kk[u][j], f[j]);
+        st_shared_u32_if(my_key_s + 4u * pos, __float_as_uint(xx[u][j]), f[j]);   // raw bits
         st_shared_u32_if(my_idx_s + 4u * pos, (uint32_t)(e + j), f[j]);
         pos += f[j];
       }
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(kTopkThreads, 5) topk_kernel(const float* __re
 #pragma unroll
           for (int w = 1; w < kTopkWarps; ++w)
             if (i >= pre[w]) src = i - pre[w] + w * kWarpCap;
-          kv[j] = cand_key[src];
+          kv[j] = order_key(__uint_as_float(cand_key[src]));   // raw bits -> key
           iv[j] = cand_idx[src];
         }
       }
