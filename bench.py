@@ -389,16 +389,26 @@ def inputs_digest(host: dict, names) -> str:
     return h.hexdigest()
 
 
+ARM_PARTS = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+             "0xd49": "Arm Neoverse-N2", "0xd84": "Arm Neoverse-V3"}
+
+
 def host_cpu() -> dict:
-    """The host's logical CPU count and a model string (best effort)."""
+    """The host's logical CPU count and a model string (best effort; Arm
+    hosts list only implementer and part numbers in /proc/cpuinfo)."""
     model = platform.processor() or platform.machine()
     try:
         with open("/proc/cpuinfo") as f:
+            fields = {}
             for ln in f:
-                key = ln.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware"):
-                    model = ln.split(":", 1)[1].strip()
-                    break
+                if ":" in ln:
+                    key, val = (x.strip() for x in ln.split(":", 1))
+                    fields.setdefault(key.lower(), val)
+        if "model name" in fields:
+            model = fields["model name"]
+        elif "cpu part" in fields:
+            part = fields["cpu part"].lower()
+            model = f"{ARM_PARTS.get(part, 'Arm CPU part ' + part)} ({platform.machine()})"
     except OSError:
         pass
     return {"host_cpus": os.cpu_count(), "cpu_model": model}
