@@ -344,20 +344,33 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
           bulk_wait_read0_if(lane < 16);
           __syncwarp();
         }
+        // two 16-column blocks per iteration: four independent MMAs before
+        // their results are stored
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-          const int ch = 2 * j + (mtx >> 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(bsrc + hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4), b0, b1, b2, b3);
-          float c2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          mma_f16_16816(c2[0], a0, a1, a2, a3, b0, b1);
-          mma_f16_16816(c2[1], a0, a1, a2, a3, b2, b3);
+        for (int j = 0; j < D / 16; j += 2) {
+          uint32_t b[2][4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t off = (uint32_t)((2 * j + h) * 32);   // columns (2j+h)*8 + 2qi, +1
-            st_shared_v2(frag + off, c2[h][0], c2[h][1]);
-            st_shared_v2(frag + 8 * C::RED_PITCH + off, c2[h][2], c2[h][3]);
+          for (int u = 0; u < 2; ++u) {
+            const int ch = 2 * (j + u) + (mtx >> 1);
+            ldsm_x4_t(bsrc + hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4), b[u][0], b[u][1], b[u][2], b[u][3]);
           }
+          float c2[2][2][4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) c2[u][h][e] = 0.f;
+              mma_f16_16816(c2[u][h], a0, a1, a2, a3, b[u][2 * h], b[u][2 * h + 1]);
+            }
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t off = (uint32_t)((2 * (j + u) + h) * 32);   // columns (2(j+u)+h)*8 + 2qi, +1
+              st_shared_v2(frag + off, c2[u][h][0], c2[u][h][1]);
+              st_shared_v2(frag + 8 * C::RED_PITCH + off, c2[u][h][2], c2[u][h][3]);
+            }
         }
         fence_proxy_async_shared();   // the tile's generic-proxy writes before the bulk reads
         __syncwarp();
