@@ -79,6 +79,9 @@ def test_null_and_misaligned_pointers_fail_before_launch(lib):
     assert b"aligned" in lib.dsa_last_error_message()
     assert lib.dsa_indexer_score(ctypes.byref(d), 256, 256, 256, 4000, 200, 256, None) == dsa.DSA_ERR_INVALID_ARG
     assert lib.dsa_topk(ctypes.byref(d), 256, -1, 10, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    # an empty query range is an error, not a silent no-op
+    assert lib.dsa_topk(ctypes.byref(d), 256, 0, 0, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_score(ctypes.byref(d), 256, 256, 256, 8, 0, 256, None) == dsa.DSA_ERR_INVALID_ARG
     # too small a workspace is reported as such
     p = ctypes.c_void_p(256)
     assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, None, p, p, p, 16, None) == \

@@ -140,9 +140,12 @@ def _topk_case(P, rows, k, kind, seed):
 
 
 @pytest.mark.parametrize("kind", ["normal", "ties", "signed_zero"])
-@pytest.mark.parametrize("k", [64, 512])
+@pytest.mark.parametrize("k", [64, 512, 1024])
 def test_topk_bitexact(kind, k):
-    L = 4 * 14000          # rows up to 14000 pools: both sides of the 12288-score staging limit
+    # rows of fewer than k pools (all kept), of up to 4096 pools (every score a
+    # candidate) and of up to 14000 pools (sampled threshold); k = 1024 is the
+    # largest k the library accepts
+    L = 4 * 14000
     P = L // 4
     dims = dsa.make_dims(L, 16, 128, 8, 64, k)
     for (q_begin, q_count) in ((0, 300), (2000, 97), (L - 40, 40), (4 * 12288 - 20, 40)):

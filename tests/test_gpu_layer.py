@@ -72,6 +72,45 @@ def test_tiny_fp32_forward_in_full():
     assert np.abs(out["lse"].cpu().numpy() - LSE).max() <= 1e-4
 
 
+@pytest.mark.parametrize("L", [4, 8, 12, 16, 132])
+@pytest.mark.parametrize("k", [1, 512])
+def test_tiny_sequences_fwd_bwd(L, k):
+    """Degenerate lengths: a single pool (L=4), score rows narrower than one
+    score tile or TMA box, a ragged last pool tile; k above and below the
+    number of eligible pools.  Compared in full with the oracle."""
+    wl = dsa_inputs.WORKLOADS["bf16_32k"].with_(name=f"bf16_tiny_{L}", L=L, k=k, q_chunk=L, indexer="int3",
+                                                  weights="int1_4")
+    host = dsa_inputs.make(wl)
+    f = {n: _f32(t) for n, t in host.items()}
+    kp = oracle.pool_keys(f["k_I"], True)
+    idx = oracle.select_rows(f["q_I"], kp, f["w"], k, None, threads=1)
+    O, LSE = oracle.attn_fwd(f["Q"], f["K"], f["V"], idx, wl.scale)
+    dQ, dK, dV = oracle.attn_bwd(f["Q"], f["K"], f["V"], idx, f["dO"], wl.scale, threads=1)
+    out = _run_layer(wl, host, with_bwd=True, o_acc=True)
+    assert np.array_equal(_f32(out["kpool"]).view(np.uint32), kp.view(np.uint32))
+    assert np.array_equal(out["idx"].cpu().numpy(), idx)
+    assert np.abs(_f32(out["o"]) - O).max() <= 2e-2
+    assert np.abs(out["o_acc"].cpu().numpy() - O).max() <= 1e-4
+    assert np.abs(out["lse"].cpu().numpy() - LSE).max() <= 1e-3
+    for n, ref in (("dq", dQ), ("dk", dK), ("dv", dV)):
+        assert np.abs(out[n].cpu().numpy() - ref).max() <= 2e-2, n
+
+
+@pytest.mark.parametrize("L", [4, 8, 132])
+def test_tiny_sequences_fp32_forward(L):
+    wl = dsa_inputs.WORKLOADS["tiny_fp32_fwd"].with_(name=f"fp32_tiny_{L}", L=L, q_chunk=L)
+    host = dsa_inputs.make(wl, ("Q", "K", "V", "q_I", "k_I", "w"))
+    f = {n: _f32(t) for n, t in host.items()}
+    kp = oracle.pool_keys(f["k_I"], False)
+    idx = oracle.select_rows(f["q_I"], kp, f["w"], wl.k, None, threads=1)
+    O, LSE = oracle.attn_fwd(f["Q"], f["K"], f["V"], idx, wl.scale)
+    out = _run_layer(wl, host, with_bwd=False, o_acc=True)
+    assert np.array_equal(out["idx"].cpu().numpy(), idx)
+    assert np.abs(_f32(out["o"]) - O).max() <= 1e-4
+    assert torch.equal(out["o_acc"], out["o"])
+    assert np.abs(out["lse"].cpu().numpy() - LSE).max() <= 1e-4
+
+
 def _bf16_multichunk():
     return dsa_inputs.WORKLOADS["bf16_32k"].with_(name="bf16_8k_int", L=8192, q_chunk=3000, indexer="int3",
                                                   weights="int1_4")
