@@ -157,10 +157,10 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   static_assert(C::NST == 2, "the pool ring below is written for two stages");
   const GatherLane<D> gl = gather_lane<D>(lane);
   const int nsteps = ngroups;
-  int pc[4];
+  uint32_t pc[4];   // packed pool slots (gather.cuh)
   bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
   step_pools(irow, k, 0, t, pc, bad_idx);
-  gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
+  gather_step16<D>(wbase, K, V, pc, gl);
   cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
   if (PASS == 2) {
@@ -196,9 +196,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
 
   for (int step = 0; step < nsteps; ++step) {
     constexpr bool pass1 = PASS == 1;
-    const int grp = step;
     const int stage = step & 1;
-    int pf[4] = {-1, -1, -1, -1};
+    uint32_t pf[4] = {0u, 0u, 0u, 0u};
     {
       const int nx = step + 1;
       if (nx < nsteps) {
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         }
         const int grp_n = nx;
         step_pools(irow, k, grp_n, t, pf, bad_idx);
-        gather_step16<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl, t, k, grp_n);
+        gather_step16<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl);
       }
       cp_async_commit();
     }
@@ -218,9 +217,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     bool kv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const int sig = nt * 2 + (qi >> 1);
-      const int pool = (qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2];
-      const int nrows = slot_rows(pool, grp * 4 + sig, k, t);
+      const int nrows = slot_nrows((qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2]);   // slot nt*2 + (qi >> 1)
 #pragma unroll
       for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
     }
@@ -331,9 +328,9 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       const uint32_t frag = tile + g * C::RED_PITCH + 8 * qi;   // this lane's (row g, columns 2qi..) slot
       // the row this lane reduces (lanes 0..15): key lane of the step
       const int rsig = (lane >> 2) & 3, rrow = lane & 3;
-      const int rpool = rsig == 0 ? pc[0] : rsig == 1 ? pc[1] : rsig == 2 ? pc[2] : pc[3];
-      const bool rok = lane < 16 && rrow < slot_rows(rpool, grp * 4 + rsig, k, t);
-      const int64_t rrow_g = 4 * (int64_t)(rpool < 0 ? 0 : rpool) + rrow;
+      const uint32_t rslot = rsig == 0 ? pc[0] : rsig == 1 ? pc[1] : rsig == 2 ? pc[2] : pc[3];
+      const bool rok = lane < 16 && rrow < slot_nrows(rslot);
+      const int64_t rrow_g = 4 * (int64_t)slot_pool(rslot) + rrow;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV = P^T dO, 1: dK = (scale dS)^T Q
         const uint32_t bsrc = which ? qs : dos;

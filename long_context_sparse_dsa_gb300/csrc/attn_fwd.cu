@@ -91,28 +91,28 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   // pools of the current step (pc) and, with three stages, of the next (pn)
-  int pc[4], pn[4] = {-1, -1, -1, -1};
+  uint32_t pc[4], pn[4] = {0u, 0u, 0u, 0u};   // packed pool slots (gather.cuh)
   bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
   step_pools(irow, k, 0, t, pc, bad_idx);
-  gather_step16<D>(wbase, K, V, pc, gl, t, k, 0);
+  gather_step16<D>(wbase, K, V, pc, gl);
   cp_async_commit();
   if constexpr (NST == 3) {
     if (ngroups > 1) {
       step_pools(irow, k, 1, t, pn, bad_idx);
-      gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl, t, k, 1);
+      gather_step16<D>(wbase + C::STAGE_BYTES, K, V, pn, gl);
     }
     cp_async_commit();
   }
 
   int stage = 0;
   for (int grp = 0; grp < ngroups; ++grp) {
-    int pf[4] = {-1, -1, -1, -1};
+    uint32_t pf[4] = {0u, 0u, 0u, 0u};
     {
       const int nx = grp + NST - 1;
       if (nx < ngroups) {
         step_pools(irow, k, nx, t, pf, bad_idx);
         const int st = stage + NST - 1 >= NST ? stage - 1 : stage + NST - 1;
-        gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl, t, k, nx);
+        gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl);
       }
       cp_async_commit();
     }
@@ -120,9 +120,8 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     bool kv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const int sig = nt * 2 + (qi >> 1);
-      const int pool = (qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2];   // no dynamic register indexing
-      const int nrows = slot_rows(pool, grp * 4 + sig, k, t);
+      // slot nt*2 + (qi >> 1), without dynamic register indexing
+      const int nrows = slot_nrows((qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2]);
 #pragma unroll
       for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
     }

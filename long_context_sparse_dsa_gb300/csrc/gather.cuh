@@ -60,15 +60,19 @@ __device__ __forceinline__ GatherLane<D> gather_lane(int lane) {
   return g;
 }
 
-// The 4 pools of step `grp` (slots grp*4 .. grp*4+3; slot k is the own partial
-// pool, -1 when there is none).  Every lane reads the 4 idx entries itself
-// (the same addresses across the warp: broadcast loads) and decides with
-// selects, so no lane-divergent branch is taken.  An entry outside the causal
-// range is skipped (-1) and sets `bad`, which the caller reports once.
-__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, int (&pools)[4],
+// The 4 pool slots of step `grp` (slots grp*4 .. grp*4+3; slot k is the own
+// partial pool), each packed as (pool << 3) | visible rows: 4 for a selected
+// pool, (t & 3) + 1 for the partial pool, and the value 0 (pool 0, no rows)
+// for an empty slot, so that an empty slot still names a valid address and
+// its rows are zero-filled.  Every lane reads the 4 idx entries itself (the
+// same addresses across the warp: broadcast loads) and decides with selects,
+// so no lane-divergent branch is taken.  An entry outside the causal range is
+// skipped and sets `bad`, which the caller reports once.
+__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, uint32_t (&slots)[4],
                                            bool& bad) {
   const int el = (int)elig(t);
-  const int part = (t & 3) != 3 ? (int)(t >> 2) : -1;
+  const bool has_part = (t & 3) != 3;
+  const uint32_t part = ((uint32_t)(t >> 2) << 3) | (uint32_t)((t & 3) + 1);
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const int slot = grp * 4 + s;
@@ -76,31 +80,24 @@ __device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, 
     const int raw = __ldg(irow + (sel ? slot : 0));   // a valid address either way (k >= 1)
     const bool out = sel && raw >= el;
     bad |= out;
-    pools[s] = sel ? ((raw < 0 || out) ? -1 : raw) : (slot == k ? part : -1);
+    const uint32_t mine = (raw < 0 || out) ? 0u : (((uint32_t)raw << 3) | 4u);
+    slots[s] = sel ? mine : ((slot == k && has_part) ? part : 0u);
   }
 }
-
-// Number of visible tokens of slot s (4 for a selected pool, 1..3 for the
-// partial pool, 0 for an empty slot).  `pool` is what step_pools gave for
-// the slot, so the partial pool (slot k) is t/4 and holds tokens 4*(t/4)..t.
-__device__ __forceinline__ int slot_rows(int pool, int slot, int k, int64_t t) {
-  if (pool < 0) return 0;
-  if (slot != k) return 4;
-  return (int)(t & 3) + 1;
-}
+__device__ __forceinline__ int slot_pool(uint32_t v) { return (int)(v >> 3); }
+__device__ __forceinline__ int slot_nrows(uint32_t v) { return (int)(v & 7u); }
 
 template <int D>
 __device__ __forceinline__ void gather_step16(uint32_t stage, const __nv_bfloat16* __restrict__ K,
-                                              const __nv_bfloat16* __restrict__ V, const int (&pools)[4],
-                                              const GatherLane<D>& gl, int64_t t, int k, int grp) {
+                                              const __nv_bfloat16* __restrict__ V, const uint32_t (&slots)[4],
+                                              const GatherLane<D>& gl) {
   using C = GatherCfg<D>;
   constexpr int NRB = GatherLane<D>::NRB;
   constexpr int POOL_BYTES = 4 * C::ROW_BYTES;
 #pragma unroll
   for (int sig = 0; sig < 4; ++sig) {
-    const int p = pools[sig];
-    const int nrows = slot_rows(p, grp * 4 + sig, k, t);
-    const int64_t pool_off = (int64_t)(p < 0 ? 0 : p) * POOL_BYTES + gl.src_off;   // a valid address even if unused
+    const int nrows = slot_nrows(slots[sig]);
+    const int64_t pool_off = (int64_t)slot_pool(slots[sig]) * POOL_BYTES + gl.src_off;
     const char* srcK = reinterpret_cast<const char*>(K) + pool_off;
     const char* srcV = reinterpret_cast<const char*>(V) + pool_off;
 #pragma unroll
