@@ -64,25 +64,24 @@ __device__ __forceinline__ GatherLane<D> gather_lane(int lane) {
 // partial pool), each packed as (pool << 3) | visible rows: 4 for a selected
 // pool, (t & 3) + 1 for the partial pool, and the value 0 (pool 0, no rows)
 // for an empty slot, so that an empty slot still names a valid address and
-// its rows are zero-filled.  Every lane reads the 4 idx entries itself (the
-// same addresses across the warp: broadcast loads) and decides with selects,
-// so no lane-divergent branch is taken.  An entry outside the causal range is
-// skipped and sets `bad`, which the caller reports once.
+// its rows are zero-filled.  Each lane decides slot (lane & 3) with selects
+// (no lane-divergent branch), and the four results are shuffled to every
+// lane.  An entry outside the causal range is skipped and sets `bad`, which
+// the caller reports once.
 __device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, uint32_t (&slots)[4],
                                            bool& bad) {
   const int el = (int)elig(t);
   const bool has_part = (t & 3) != 3;
   const uint32_t part = ((uint32_t)(t >> 2) << 3) | (uint32_t)((t & 3) + 1);
+  const int slot = grp * 4 + (int)(threadIdx.x & 3);
+  const bool sel = slot < k;
+  const int raw = __ldg(irow + (sel ? slot : 0));   // a valid address either way (k >= 1)
+  const bool out = sel && raw >= el;
+  bad |= out;
+  const uint32_t mine =
+      sel ? ((raw < 0 || out) ? 0u : (((uint32_t)raw << 3) | 4u)) : ((slot == k && has_part) ? part : 0u);
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int slot = grp * 4 + s;
-    const bool sel = slot < k;
-    const int raw = __ldg(irow + (sel ? slot : 0));   // a valid address either way (k >= 1)
-    const bool out = sel && raw >= el;
-    bad |= out;
-    const uint32_t mine = (raw < 0 || out) ? 0u : (((uint32_t)raw << 3) | 4u);
-    slots[s] = sel ? mine : ((slot == k && has_part) ? part : 0u);
-  }
+  for (int s = 0; s < 4; ++s) slots[s] = __shfl_sync(0xffffffffu, mine, s);
 }
 __device__ __forceinline__ int slot_pool(uint32_t v) { return (int)(v >> 3); }
 __device__ __forceinline__ int slot_nrows(uint32_t v) { return (int)(v & 7u); }
@@ -104,6 +103,40 @@ __device__ __forceinline__ void gather_step16(uint32_t stage, const __nv_bfloat1
     for (int rb = 0; rb < NRB; ++rb) {
       const uint32_t bytes = rb * C::ROWS_PER_COPY + gl.row_lo < nrows ? 16u : 0u;
       const uint32_t dst = stage + sig * POOL_BYTES + gl.dst_off[sig & 1][rb];
+      cp_async16(dst, srcK + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
+      cp_async16(dst + C::TILE_BYTES, srcV + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
+    }
+  }
+}
+
+// The same 16-key gather into a pool-interleaved tile: shared row m holds
+// token (m >> 2) of slot (m & 3), so that row m of the tile, and column m of
+// any product formed from it, belongs to slot m & 3.  The swizzle is the
+// usual one (chunk c of row m at c ^ (m & 7)).  Since a lane's rows all have
+// the same parity, (m & 7) = ((row & 1) << 2) | slot and the destination is a
+// lane constant plus compile-time offsets, XOR the slot.
+template <int D>
+__device__ __forceinline__ void gather_step16_il(uint32_t stage, const __nv_bfloat16* __restrict__ K,
+                                                 const __nv_bfloat16* __restrict__ V, const uint32_t (&slots)[4],
+                                                 const GatherLane<D>& gl) {
+  using C = GatherCfg<D>;
+  constexpr int NRB = GatherLane<D>::NRB;
+  constexpr int POOL_BYTES = 4 * C::ROW_BYTES;
+  const int ch = (int)((gl.src_off % C::ROW_BYTES) >> 4);
+  const uint32_t cpar = (uint32_t)(ch ^ ((gl.row_lo & 1) << 2));   // chunk position before the slot XOR
+  const uint32_t row_base = stage + (uint32_t)(gl.row_lo * 4 * C::ROW_BYTES);
+#pragma unroll
+  for (int sig = 0; sig < 4; ++sig) {
+    const int nrows = slot_nrows(slots[sig]);
+    const int64_t pool_off = (int64_t)slot_pool(slots[sig]) * POOL_BYTES + gl.src_off;
+    const char* srcK = reinterpret_cast<const char*>(K) + pool_off;
+    const char* srcV = reinterpret_cast<const char*>(V) + pool_off;
+    const uint32_t col = (cpar ^ (uint32_t)sig) << 4;
+#pragma unroll
+    for (int rb = 0; rb < NRB; ++rb) {
+      const uint32_t bytes = rb * C::ROWS_PER_COPY + gl.row_lo < nrows ? 16u : 0u;
+      // token row = rb*ROWS_PER_COPY + row_lo  ->  shared row 4*row + sig
+      const uint32_t dst = row_base + (uint32_t)((rb * C::ROWS_PER_COPY * 4 + sig) * C::ROW_BYTES) + col;
       cp_async16(dst, srcK + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
       cp_async16(dst + C::TILE_BYTES, srcV + rb * C::ROWS_PER_COPY * C::ROW_BYTES, bytes);
     }
