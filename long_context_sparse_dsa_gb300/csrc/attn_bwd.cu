@@ -44,17 +44,18 @@ struct BwdCfg {
   static constexpr int CHUNKS = GatherCfg<D>::CHUNKS;
   static constexpr int TILE_BYTES = GatherCfg<D>::TILE_BYTES;
   static constexpr int STAGE_BYTES = GatherCfg<D>::STAGE_BYTES;
-  // A consumed stage also holds a 16-key fp32 dK or dV tile with rows RED_PITCH
-  // bytes apart (a row of D fp32 plus 32 bytes, which keeps the fragment
-  // writes free of bank conflicts), so each stage is followed by padding.
+  // A consumed stage also holds a 16-key fp32 dK or dV tile as four pool
+  // blocks POOL_PITCH bytes apart, each the pool's four rows back to back (one
+  // contiguous bulk reduction per pool); the 32 bytes between blocks keep the
+  // fragment writes free of bank conflicts.  Each stage is padded to fit it.
   static constexpr int RED_ROW = D * 4;
-  static constexpr int RED_PITCH = RED_ROW + 32;
-  static constexpr int STAGE_PITCH = 16 * RED_PITCH > STAGE_BYTES ? 16 * RED_PITCH : STAGE_BYTES;
+  static constexpr int POOL_PITCH = 4 * RED_ROW + 32;
+  static constexpr int STAGE_PITCH = 4 * POOL_PITCH > STAGE_BYTES ? 4 * POOL_PITCH : STAGE_BYTES;
   static constexpr int NST = 2;
   static constexpr int WARPS = 4;
   static constexpr int WARP_BYTES = NST * STAGE_PITCH + (PASS == 2 ? 2 * TILE_BYTES : 0);
   static constexpr int SMEM = WARPS * WARP_BYTES;
-  static_assert(STAGE_PITCH % 16 == 0 && WARP_BYTES % 16 == 0 && RED_PITCH % 16 == 0, "16-byte alignment");
+  static_assert(STAGE_PITCH % 16 == 0 && WARP_BYTES % 16 == 0 && POOL_PITCH % 16 == 0, "16-byte alignment");
 };
 
 // Bulk (TMA-engine) fp32 add of `bytes` contiguous shared-memory bytes into
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   uint32_t pc[4];   // packed pool slots (gather.cuh)
   bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
   step_pools(irow, k, 0, t, pc, bad_idx);
-  gather_step16<D>(wbase, K, V, pc, gl);
+  gather_step16_il<D>(wbase, K, V, pc, gl);
   cp_async_commit();
   float Dg = 0.f, Dg8 = 0.f;
   if (PASS == 2) {
@@ -204,12 +205,12 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         // the stage being refilled held the previous step's dK tile: its bulk
         // reductions must have finished reading it
         if (PASS == 2) {
-          bulk_wait_read0_if(lane < 16);
+          bulk_wait_read0_if(lane < 4);
           __syncwarp();
         }
         const int grp_n = nx;
         step_pools(irow, k, grp_n, t, pf, bad_idx);
-        gather_step16<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl);
+        gather_step16_il<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl);
       }
       cp_async_commit();
     }
@@ -217,9 +218,13 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     bool kv[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const int nrows = slot_nrows((qi >> 1) ? pc[nt * 2 + 1] : pc[nt * 2]);   // slot nt*2 + (qi >> 1)
+      // the tile is pool-interleaved: column n = nt*8 + 2qi + e is token n >> 2
+      // of slot n & 3 = 2(qi & 1) + e
 #pragma unroll
-      for (int e = 0; e < 2; ++e) kv[nt][e] = 2 * (qi & 1) + e < nrows;
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t sl = (qi & 1) ? (e ? pc[3] : pc[2]) : (e ? pc[1] : pc[0]);
+        kv[nt][e] = 2 * nt + (qi >> 1) < slot_nrows(sl);
+      }
     }
     cp_async_wait<C::NST - 1>();
     __syncwarp();
@@ -315,22 +320,25 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     const uint32_t dt0 = movmatrix_t(dh[0][0]), dt1 = movmatrix_t(dh[1][0]);
     const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
     // The step's K/V stage is free now (S, dP and dQ are done).  Each 16-key
-    // fp32 tile (dV, then dK) is written into it in fragment order, row r at
-    // r * RED_PITCH: the 32-byte row padding puts the 8 rows of one fragment
-    // write in distinct bank groups.  Then lanes 0..15 each hand one visible
-    // key row (D fp32, contiguous) to the TMA engine as one bulk fp32
-    // reduction into global memory.
+    // fp32 tile (dV, then dK) is written into it in fragment order: tile row m
+    // (token m >> 2 of slot m & 3) at (m & 3) * POOL_PITCH + (m >> 2) * RED_ROW,
+    // so the 8 rows of one fragment write fall in 4 pool blocks whose 32-byte
+    // offsets put them in distinct bank groups, and each pool's rows are one
+    // contiguous run.  Lanes 0..3 then hand one pool each (its visible rows)
+    // to the TMA engine as one bulk fp32 reduction into global memory.
     __syncwarp();
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int hrow = (mtx & 1) * 8 + r;
       const uint32_t tile = ks_base;
-      const uint32_t frag = tile + g * C::RED_PITCH + 8 * qi;   // this lane's (row g, columns 2qi..) slot
-      // the row this lane reduces (lanes 0..15): key lane of the step
-      const int rsig = (lane >> 2) & 3, rrow = lane & 3;
-      const uint32_t rslot = rsig == 0 ? pc[0] : rsig == 1 ? pc[1] : rsig == 2 ? pc[2] : pc[3];
-      const bool rok = lane < 16 && rrow < slot_nrows(rslot);
-      const int64_t rrow_g = 4 * (int64_t)slot_pool(rslot) + rrow;
+      // this lane's fragment rows g and g+8 (tile rows m = g, g+8), columns 2qi..
+      const uint32_t frag = tile + (g & 3) * C::POOL_PITCH + (g >> 2) * C::RED_ROW + 8 * qi;
+      // the pool this lane reduces (lanes 0..3): slot `lane`
+      const uint32_t rslot = (lane & 3) == 0 ? pc[0] : (lane & 3) == 1 ? pc[1] : (lane & 3) == 2 ? pc[2] : pc[3];
+      const bool rok = lane < 4 && slot_nrows(rslot) > 0;
+      const int64_t rrow_g = 4 * (int64_t)slot_pool(rslot);
+      const uint32_t rbytes = (uint32_t)(slot_nrows(rslot) * C::RED_ROW);
+      const uint32_t rsrc = tile + (lane & 3) * C::POOL_PITCH;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV = P^T dO, 1: dK = (scale dS)^T Q
         const uint32_t bsrc = which ? qs : dos;
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         const uint32_t a2 = which ? dt2 : pt2, a3 = which ? dt3 : pt3;
         if (which == 1) {
           // the dV tile's reductions must have read it before dK overwrites it
-          bulk_wait_read0_if(lane < 16);
+          bulk_wait_read0_if(lane < 4);
           __syncwarp();
         }
         // two 16-column blocks per iteration: four independent MMAs before
@@ -366,13 +374,13 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
             for (int h = 0; h < 2; ++h) {
               const uint32_t off = (uint32_t)((2 * (j + u) + h) * 32);   // columns (2(j+u)+h)*8 + 2qi, +1
               st_shared_v2(frag + off, c2[u][h][0], c2[u][h][1]);
-              st_shared_v2(frag + 8 * C::RED_PITCH + off, c2[u][h][2], c2[u][h][3]);
+              st_shared_v2(frag + 2 * C::RED_ROW + off, c2[u][h][2], c2[u][h][3]);   // row g+8: token +2
             }
         }
         fence_proxy_async_shared();   // the tile's generic-proxy writes before the bulk reads
         __syncwarp();
         float* gdst = which ? dK : dV;
-        bulk_red_add_f32_if(gdst + rrow_g * D, tile + (lane & 15) * C::RED_PITCH, (uint32_t)C::RED_ROW, rok);
+        bulk_red_add_f32_if(gdst + rrow_g * D, rsrc, rbytes, rok);
       }
     }
     __syncwarp();
