@@ -38,6 +38,14 @@ namespace dsa {
 
 // PASS 1 forms D[t,h] = sum_j P_j dP_j into a [L, Hq] fp32 buffer; PASS 2
 // forms dS and the gradients.  PASS 2 also keeps fp16 copies of Q and dO.
+// Gather stages per warp and warps per CTA (two CTAs per SM either way:
+// shared memory allows 2 x 4 warps x 2 stages or 2 x 3 warps x 3 stages).
+// Measured at L=131072: 45.8 ms for two stages at four warps, 46.6 ms for
+// three stages at three warps -- the extra tile in flight does not make up
+// for a quarter fewer warps.
+constexpr int kBwdStages = 2;
+constexpr int kBwdWarps = 4;
+
 template <int D, int PASS>
 struct BwdCfg {
   static constexpr int ROW_BYTES = GatherCfg<D>::ROW_BYTES;
@@ -51,12 +59,26 @@ struct BwdCfg {
   static constexpr int RED_ROW = D * 4;
   static constexpr int POOL_PITCH = 4 * RED_ROW + 32;
   static constexpr int STAGE_PITCH = 4 * POOL_PITCH > STAGE_BYTES ? 4 * POOL_PITCH : STAGE_BYTES;
-  static constexpr int NST = 2;
-  static constexpr int WARPS = 4;
+  static constexpr int NST = kBwdStages;      // gather stages per warp (2 or 3)
+  static constexpr int WARPS = kBwdWarps;     // warps (queries) per CTA
   static constexpr int WARP_BYTES = NST * STAGE_PITCH + (PASS == 2 ? 2 * TILE_BYTES : 0);
   static constexpr int SMEM = WARPS * WARP_BYTES;
   static_assert(STAGE_PITCH % 16 == 0 && WARP_BYTES % 16 == 0 && POOL_PITCH % 16 == 0, "16-byte alignment");
 };
+
+// Advance the pool-slot ring by one step: current <- next (<- fetched).
+template <int NST>
+__device__ __forceinline__ void rotate_slots(uint32_t (&pc)[4], uint32_t (&pn)[4], const uint32_t (&pf)[4]) {
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    if constexpr (NST == 3) {
+      pc[s4] = pn[s4];
+      pn[s4] = pf[s4];
+    } else {
+      pc[s4] = pf[s4];
+    }
+  }
+}
 
 // Bulk (TMA-engine) fp32 add of `bytes` contiguous shared-memory bytes into
 // global memory, then a commit of this thread's bulk group; both only where
@@ -87,7 +109,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
 }
 
 template <int D, int PASS>
-__global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
+__global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
     const int32_t* __restrict__ idx, const float* __restrict__ LSE, const __nv_bfloat16* __restrict__ dO,
     const float* __restrict__ Oacc, float* __restrict__ Dbuf, float* __restrict__ dQ, float* __restrict__ dK,
@@ -155,14 +177,22 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
   // One pass over the key groups.  PASS 1 accumulates D[h] = sum_j P_j dP_j
   // (equal to dO . O, but from the exact P and dP rather than the
   // bf16-rounded O); PASS 2 reads it back and forms dS and the gradients.
-  static_assert(C::NST == 2, "the pool ring below is written for two stages");
+  static_assert(C::NST == 2 || C::NST == 3, "the pool ring below is written for two or three stages");
   const GatherLane<D> gl = gather_lane<D>(lane);
   const int nsteps = ngroups;
-  uint32_t pc[4];   // packed pool slots (gather.cuh)
+  // packed pool slots (gather.cuh) of the current step and, with three stages, the next
+  uint32_t pc[4], pn[4] = {0u, 0u, 0u, 0u};
   bool bad_idx = false;   // an idx entry outside the causal range (skipped, reported once)
   step_pools(irow, k, 0, t, pc, bad_idx);
   gather_step16_il<D>(wbase, K, V, pc, gl);
   cp_async_commit();
+  if constexpr (C::NST == 3) {
+    if (nsteps > 1) {
+      step_pools(irow, k, 1, t, pn, bad_idx);
+      gather_step16_il<D>(wbase + C::STAGE_PITCH, K, V, pn, gl);
+    }
+    cp_async_commit();
+  }
   float Dg = 0.f, Dg8 = 0.f;
   if (PASS == 2) {
     if (Oacc != nullptr) {
@@ -195,22 +225,22 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
     }
   }
 
+  int stage = 0;
   for (int step = 0; step < nsteps; ++step) {
     constexpr bool pass1 = PASS == 1;
-    const int stage = step & 1;
     uint32_t pf[4] = {0u, 0u, 0u, 0u};
     {
-      const int nx = step + 1;
+      const int nx = step + C::NST - 1;
       if (nx < nsteps) {
-        // the stage being refilled held the previous step's dK tile: its bulk
-        // reductions must have finished reading it
+        // the stage being refilled is the one the previous step consumed and
+        // staged its dK tile in: those bulk reductions must have read it
         if (PASS == 2) {
           bulk_wait_read0_if(lane < 4);
           __syncwarp();
         }
-        const int grp_n = nx;
-        step_pools(irow, k, grp_n, t, pf, bad_idx);
-        gather_step16_il<D>(wbase + (nx & 1) * C::STAGE_PITCH, K, V, pf, gl);
+        const int st = stage == 0 ? C::NST - 1 : stage - 1;
+        step_pools(irow, k, nx, t, pf, bad_idx);
+        gather_step16_il<D>(wbase + st * C::STAGE_PITCH, K, V, pf, gl);
       }
       cp_async_commit();
     }
@@ -279,8 +309,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
         Dg8 = fmaf(ex2_approx(kv[nt][1] ? s[nt][3] * scale_log2 - lse_g8 : -INFINITY), dp[nt][3], Dg8);
       }
       __syncwarp();
-#pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
+      rotate_slots<C::NST>(pc, pn, pf);
+      stage = stage == C::NST - 1 ? 0 : stage + 1;
       continue;
     }
     // P and scale*dS: bf16 for the dQ product, fp16 for dK/dV (rows g: elements 0,1; rows g+8: 2,3)
@@ -384,8 +414,8 @@ __global__ void __launch_bounds__(128) attn_bwd_bf16_kernel(
       }
     }
     __syncwarp();
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) pc[s4] = pf[s4];
+    rotate_slots<C::NST>(pc, pn, pf);
+    stage = stage == C::NST - 1 ? 0 : stage + 1;
   }
   cp_async_wait<0>();
   if (PASS == 2) {
