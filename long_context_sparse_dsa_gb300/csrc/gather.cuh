@@ -7,10 +7,11 @@
 // position c ^ (r & 7), which makes the ldmatrix reads conflict-free.
 //
 // Everything that depends only on the lane is computed once (GatherLane);
-// per step a lane needs the 4 pool indices of the step (broadcast loads),
-// one address per pool slot, and then one compare per copy.  Keys that
-// are not visible (empty slot, or tokens after t in the partial pool) are
-// zero-filled.
+// per step a lane reads one idx entry (the step's 4 packed pool slots then
+// reach every lane by shuffles), forms one address per pool slot, and then
+// one compare per copy.  Keys that are not visible (empty slot, or tokens
+// after t in the partial pool) are zero-filled.  The backward uses a
+// pool-interleaved variant of the tile (gather_step16_il).
 #pragma once
 
 #include "common.cuh"
