@@ -158,14 +158,17 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
     }
-    // online softmax (log2 domain); c0,c1 -> head g, c2,c3 -> head g+8
+    // online softmax (log2 domain); c0,c1 -> head g, c2,c3 -> head g+8.  The
+    // scores stay unscaled (invisible keys masked to -inf) and the scale
+    // enters with the exponent: p = 2^(s * scale_log2 - base), one FMA; the
+    // step max is scaled once (scale > 0 keeps the order).
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = kv[nt][0] ? s[nt][0] * scale_log2 : -INFINITY;
-      s[nt][1] = kv[nt][1] ? s[nt][1] * scale_log2 : -INFINITY;
-      s[nt][2] = kv[nt][0] ? s[nt][2] * scale_log2 : -INFINITY;
-      s[nt][3] = kv[nt][1] ? s[nt][3] * scale_log2 : -INFINITY;
+      s[nt][0] = kv[nt][0] ? s[nt][0] : -INFINITY;
+      s[nt][1] = kv[nt][1] ? s[nt][1] : -INFINITY;
+      s[nt][2] = kv[nt][0] ? s[nt][2] : -INFINITY;
+      s[nt][3] = kv[nt][1] ? s[nt][3] : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
@@ -173,6 +176,8 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    mx0 *= scale_log2;
+    mx1 *= scale_log2;
     // Lazy rescaling: the exponent base m moves only when the step's max
     // exceeds it by more than kLazyLog2 (so P <= 2^kLazyLog2 in fp32, and
     // O and l are rescaled rarely); LSE = m + log2(l) holds for any base.
@@ -185,10 +190,10 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = ex2_approx(s[nt][0] - base0);
-      s[nt][1] = ex2_approx(s[nt][1] - base0);
-      s[nt][2] = ex2_approx(s[nt][2] - base1);
-      s[nt][3] = ex2_approx(s[nt][3] - base1);
+      s[nt][0] = ex2_approx(fmaf(s[nt][0], scale_log2, -base0));
+      s[nt][1] = ex2_approx(fmaf(s[nt][1], scale_log2, -base0));
+      s[nt][2] = ex2_approx(fmaf(s[nt][2], scale_log2, -base1));
+      s[nt][3] = ex2_approx(fmaf(s[nt][3], scale_log2, -base1));
       rs0 += s[nt][0] + s[nt][1];
       rs1 += s[nt][2] + s[nt][3];
     }
