@@ -61,7 +61,7 @@ def load_peaks():
 # after any change to them the bench reports null until it is captured again.
 TRAFFIC = {
     ("bf16_128k_needle", "attn_bwd"): {"bytes": 10984459776 + 8600271616,
-                                       "sources": {"attn_bwd.cu": "d69c965b2d991305", "gather.cuh": "62f83b97f6276d92",
+                                       "sources": {"attn_bwd.cu": "3c69d9e6b31cbafd", "gather.cuh": "62f83b97f6276d92",
                                                    "common.cuh": "6fbc65a01c30f2d5"}},
     ("bf16_128k_needle", "attn_fwd"): {"bytes": 1290877184 + 1566432512,
                                        "sources": {"attn_fwd.cu": "96fb59f650f14fc8", "gather.cuh": "62f83b97f6276d92",

@@ -24,12 +24,13 @@
 // from a per-warp swizzled shared copy.  The dK/dV products run in fp16
 // (P, scale*dS, Q, dO converted; 10-bit mantissa instead of bf16's 7) because
 // those sums collect contributions from every query that selected a key.
-// Each finished 16-key dK/dV tile is staged in shared memory (rows padded so
-// the fragment writes do not conflict) and each visible key row is added to
-// global memory by one bulk fp32 reduction of the TMA engine
-// (cp.reduce.async.bulk, one contiguous row of D floats).  Row-contiguous
-// reductions are absorbed by the L2 about 1.6x faster than fragment-shaped
-// ones; the summation order across queries is not fixed.
+// The tile is gathered pool-interleaved (row m = token m >> 2 of slot m & 3),
+// so each finished 16-key dK/dV tile can be staged in shared memory as four
+// pool blocks (padded so the fragment writes do not conflict) and each pool's
+// visible rows are added to global memory by one bulk fp32 reduction of the
+// TMA engine (cp.reduce.async.bulk, up to 4*D contiguous floats).
+// Row-contiguous reductions are absorbed by the L2 about 1.6x faster than
+// fragment-shaped ones; the summation order across queries is not fixed.
 #include "common.cuh"
 #include "gather.cuh"
 #include "launch.h"
