@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
     }
   }
 
+  int raw_next = slot_raw(irow, k, C::NST - 1);   // idx entry of the first prefetch in the loop
   int stage = 0;
   for (int step = 0; step < nsteps; ++step) {
     constexpr bool pass1 = PASS == 1;
@@ -240,9 +241,10 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
           __syncwarp();
         }
         const int st = stage == 0 ? C::NST - 1 : stage - 1;
-        step_pools(irow, k, nx, t, pf, bad_idx);
+        step_pools_from(raw_next, k, nx, t, pf, bad_idx);
         gather_step16_il<D>(wbase + st * C::STAGE_PITCH, K, V, pf, gl);
       }
+      raw_next = slot_raw(irow, k, nx + 1);   // the next prefetch's idx entry, a step early
       cp_async_commit();
     }
     // visibility of this lane's S/dP columns (keys nt*8 + 2qi + e)

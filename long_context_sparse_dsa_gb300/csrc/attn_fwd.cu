@@ -104,16 +104,18 @@ __global__ void __launch_bounds__(128, MINB) attn_fwd_bf16_kernel(const __nv_bfl
     cp_async_commit();
   }
 
+  int raw_next = slot_raw(irow, k, NST - 1);   // idx entry of the first prefetch in the loop
   int stage = 0;
   for (int grp = 0; grp < ngroups; ++grp) {
     uint32_t pf[4] = {0u, 0u, 0u, 0u};
     {
       const int nx = grp + NST - 1;
       if (nx < ngroups) {
-        step_pools(irow, k, nx, t, pf, bad_idx);
+        step_pools_from(raw_next, k, nx, t, pf, bad_idx);
         const int st = stage + NST - 1 >= NST ? stage - 1 : stage + NST - 1;
         gather_step16<D>(wbase + st * C::STAGE_BYTES, K, V, pf, gl);
       }
+      raw_next = slot_raw(irow, k, nx + 1);   // the next prefetch's idx entry, a step early
       cp_async_commit();
     }
     // visibility of this lane's S columns: keys nt*8 + 2*qi + {0,1}

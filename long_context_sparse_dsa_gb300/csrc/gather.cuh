@@ -61,28 +61,39 @@ __device__ __forceinline__ GatherLane<D> gather_lane(int lane) {
   return g;
 }
 
+// The idx entry this lane decides for step `grp`: slot grp*4 + (lane & 3), or
+// 0 when that slot is past the k selected ones.  Loaded a step ahead of its
+// use, so its latency is hidden behind the current step.
+__device__ __forceinline__ int slot_raw(const int32_t* irow, int k, int grp) {
+  const int slot = grp * 4 + (int)(threadIdx.x & 3);
+  return slot < k ? __ldg(irow + slot) : 0;
+}
+
 // The 4 pool slots of step `grp` (slots grp*4 .. grp*4+3; slot k is the own
 // partial pool), each packed as (pool << 3) | visible rows: 4 for a selected
 // pool, (t & 3) + 1 for the partial pool, and the value 0 (pool 0, no rows)
 // for an empty slot, so that an empty slot still names a valid address and
-// its rows are zero-filled.  Each lane decides slot (lane & 3) with selects
-// (no lane-divergent branch), and the four results are shuffled to every
-// lane.  An entry outside the causal range is skipped and sets `bad`, which
-// the caller reports once.
-__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, uint32_t (&slots)[4],
-                                           bool& bad) {
+// its rows are zero-filled.  Each lane decides slot (lane & 3) from `raw`
+// (slot_raw of the same step) with selects (no lane-divergent branch), and
+// the four results are shuffled to every lane.  An entry outside the causal
+// range is skipped and sets `bad`, which the caller reports once.
+__device__ __forceinline__ void step_pools_from(int raw, int k, int grp, int64_t t, uint32_t (&slots)[4],
+                                                bool& bad) {
   const int el = (int)elig(t);
   const bool has_part = (t & 3) != 3;
   const uint32_t part = ((uint32_t)(t >> 2) << 3) | (uint32_t)((t & 3) + 1);
   const int slot = grp * 4 + (int)(threadIdx.x & 3);
   const bool sel = slot < k;
-  const int raw = __ldg(irow + (sel ? slot : 0));   // a valid address either way (k >= 1)
   const bool out = sel && raw >= el;
   bad |= out;
   const uint32_t mine =
       sel ? ((raw < 0 || out) ? 0u : (((uint32_t)raw << 3) | 4u)) : ((slot == k && has_part) ? part : 0u);
 #pragma unroll
   for (int s = 0; s < 4; ++s) slots[s] = __shfl_sync(0xffffffffu, mine, s);
+}
+__device__ __forceinline__ void step_pools(const int32_t* irow, int k, int grp, int64_t t, uint32_t (&slots)[4],
+                                           bool& bad) {
+  step_pools_from(slot_raw(irow, k, grp), k, grp, t, slots, bad);
 }
 __device__ __forceinline__ int slot_pool(uint32_t v) { return (int)(v >> 3); }
 __device__ __forceinline__ int slot_nrows(uint32_t v) { return (int)(v & 7u); }
