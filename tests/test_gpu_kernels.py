@@ -131,6 +131,12 @@ def _topk_case(P, rows, k, kind, seed):
     n = len(rows)
     if kind == "ties":
         s = torch.randint(-3, 4, (n, P), generator=g).to(torch.float32)
+    elif kind == "ties_spikes":
+        # integer scores plus a few larger ones per row: the k-th score has
+        # thousands of ties and some scores lie above it
+        s = torch.randint(-3, 4, (n, P), generator=g).to(torch.float32)
+        pos = torch.randint(0, P, (n, 40), generator=g)
+        s.scatter_(1, pos, 10.0)
     elif kind == "signed_zero":
         s = torch.randint(-1, 2, (n, P), generator=g).to(torch.float32) * 0.0   # +0 and -0 only
         s[:, ::17] = -1.5
@@ -139,7 +145,7 @@ def _topk_case(P, rows, k, kind, seed):
     return s
 
 
-@pytest.mark.parametrize("kind", ["normal", "ties", "signed_zero"])
+@pytest.mark.parametrize("kind", ["normal", "ties", "ties_spikes", "signed_zero"])
 @pytest.mark.parametrize("k", [64, 512, 1024])
 def test_topk_bitexact(kind, k):
     # rows of fewer than k pools (all kept), of up to 4096 pools (every score a
