@@ -62,10 +62,10 @@ def load_peaks():
 TRAFFIC = {
     ("bf16_128k_needle", "attn_bwd"): {"bytes": 11048906752 + 8431785472,
                                        "sources": {"attn_bwd.cu": "bac6e9f136e06ee9", "gather.cuh": "9c5588b13d0916cd",
-                                                   "common.cuh": "6fbc65a01c30f2d5"}},
+                                                   "common.cuh": "ccd81ae7439639d8"}},
     ("bf16_128k_needle", "attn_fwd"): {"bytes": 1273865728 + 1568081664,
                                        "sources": {"attn_fwd.cu": "ffdff854d43dc7cb", "gather.cuh": "9c5588b13d0916cd",
-                                                   "common.cuh": "6fbc65a01c30f2d5"}},
+                                                   "common.cuh": "ccd81ae7439639d8"}},
 }
 
 
