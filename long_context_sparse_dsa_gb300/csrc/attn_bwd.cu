@@ -21,9 +21,13 @@
 // the warp computes the 16x16 S and dP tiles with m16n8k16 MMAs (heads on M),
 // then the 16-key x d tiles of dK and dV with the keys on M: the transposed
 // P and dS operands are built in registers with movmatrix, and Q / dO come
-// from a per-warp swizzled shared copy.  The dK/dV products run in fp16
-// (P, scale*dS, Q, dO converted; 10-bit mantissa instead of bf16's 7) because
-// those sums collect contributions from every query that selected a key.
+// from a per-warp swizzled shared copy.  Those sums collect contributions
+// from every query that selected a key, so P and scale*dS enter the dK/dV
+// products as two bf16 terms each, x = hi + lo with hi = bf16(x) and
+// lo = bf16(x - hi) (about 2^-17 relative instead of bf16's 2^-9), against
+// the exact bf16 Q and dO.  Every operand keeps the fp32 exponent range, so
+// loss-scaled gradients (dO ~ 1e-6) and inputs beyond fp16's 65504 are
+// carried without overflow or underflow.
 // The tile is gathered pool-interleaved (row m = token m >> 2 of slot m & 3),
 // so each finished 16-key dK/dV tile can be staged in shared memory as four
 // pool blocks (padded so the fragment writes do not conflict) and each pool's
@@ -38,7 +42,7 @@
 namespace dsa {
 
 // PASS 1 forms D[t,h] = sum_j P_j dP_j into a [L, Hq] fp32 buffer; PASS 2
-// forms dS and the gradients.  PASS 2 also keeps fp16 copies of Q and dO.
+// forms dS and the gradients.  PASS 2 also keeps swizzled copies of Q and dO.
 // Gather stages per warp and warps per CTA (two CTAs per SM either way:
 // shared memory allows 2 x 4 warps x 2 stages or 2 x 3 warps x 3 stages).
 // Measured at L=131072: 45.8 ms for two stages at four warps, 46.6 ms for
@@ -99,14 +103,11 @@ __device__ __forceinline__ void bulk_wait_read0_if(bool pred) {
                : "memory");
 }
 
-// Eight bf16 values -> eight fp16 values (exact for |x| in [2^-14, 65504]).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    out[i] = pack_f16(__uint_as_float(in[i] << 16), __uint_as_float(in[i] & 0xFFFF0000u));
-  return make_uint4(out[0], out[1], out[2], out[3]);
+// x = hi + lo for two fp32 values: hi their bf16 rounding, lo the bf16
+// rounding of the (exact) fp32 remainder.
+__device__ __forceinline__ void split_bf16x2_bwd(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
 }
 
 template <int D, int PASS>
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
   const int g = lane >> 2, qi = lane & 3;
   const int64_t row0 = t * Hq + hg * 16;  // first (t, head) row of this warp
 
-  // Per-warp swizzled fp16 copies of Q and dO (16 heads x D), 16-byte chunks;
+  // Per-warp swizzled bf16 copies of Q and dO (16 heads x D), 16-byte chunks;
   // the B operands of the dK and dV products.
   if (PASS == 2) {
     const uint4* q4 = reinterpret_cast<const uint4*>(Q + row0 * D);
@@ -143,8 +144,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
     for (int c = lane; c < 16 * C::CHUNKS; c += 32) {
       const int r = c / C::CHUNKS, ch = c % C::CHUNKS;
       const int off = r * C::ROW_BYTES + ((ch ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(qsp + off) = bf16x8_to_f16x8(__ldg(q4 + c));
-      *reinterpret_cast<uint4*>(dsp + off) = bf16x8_to_f16x8(__ldg(d4 + c));
+      *reinterpret_cast<uint4*>(qsp + off) = __ldg(q4 + c);
+      *reinterpret_cast<uint4*>(dsp + off) = __ldg(d4 + c);
     }
   }
   constexpr float kLog2e = 1.4426950408889634f;
@@ -316,8 +317,9 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
       stage = stage == C::NST - 1 ? 0 : stage + 1;
       continue;
     }
-    // P and scale*dS: bf16 for the dQ product, fp16 for dK/dV (rows g: elements 0,1; rows g+8: 2,3)
-    uint32_t pp[2][2], dd[2][2], dh[2][2];
+    // P and scale*dS as bf16 hi + lo (rows g: elements 0,1; rows g+8: 2,3);
+    // the dQ product takes the hi part of scale*dS only
+    uint32_t pp[2][2], pl[2][2], dd[2][2], dl[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       // an invisible key gets 2^-inf = +0 exactly (no branch around the ex2)
@@ -327,12 +329,10 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
       const float p3 = ex2_approx(kv[nt][1] ? s[nt][3] * scale_log2 - lse_g8 : -INFINITY);
       const float s0 = scale * p0 * (dp[nt][0] - Dg), s1 = scale * p1 * (dp[nt][1] - Dg);
       const float s2 = scale * p2 * (dp[nt][2] - Dg8), s3 = scale * p3 * (dp[nt][3] - Dg8);
-      pp[nt][0] = pack_f16(p0, p1);
-      pp[nt][1] = pack_f16(p2, p3);
-      dd[nt][0] = pack_bf16(s0, s1);
-      dd[nt][1] = pack_bf16(s2, s3);
-      dh[nt][0] = pack_f16(s0, s1);
-      dh[nt][1] = pack_f16(s2, s3);
+      split_bf16x2_bwd(p0, p1, pp[nt][0], pl[nt][0]);
+      split_bf16x2_bwd(p2, p3, pp[nt][1], pl[nt][1]);
+      split_bf16x2_bwd(s0, s1, dd[nt][0], dl[nt][0]);
+      split_bf16x2_bwd(s2, s3, dd[nt][1], dl[nt][1]);
     }
     // dQ += scale*dS K   (A = dS rows=heads, B = K^T via transposed loads)
     {
@@ -348,10 +348,21 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
       }
     }
     // dV[keys] += P^T dO and dK[keys] += (scale*dS)^T Q   (rows = keys)
-    const uint32_t pt0 = movmatrix_t(pp[0][0]), pt1 = movmatrix_t(pp[1][0]);
-    const uint32_t pt2 = movmatrix_t(pp[0][1]), pt3 = movmatrix_t(pp[1][1]);
-    const uint32_t dt0 = movmatrix_t(dh[0][0]), dt1 = movmatrix_t(dh[1][0]);
-    const uint32_t dt2 = movmatrix_t(dh[0][1]), dt3 = movmatrix_t(dh[1][1]);
+    // transposed A operands (rows = keys): [0] the hi parts, [1] the lo parts
+    uint32_t pt[2][4], dt[2][4];
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const uint32_t (&ps)[2][2] = part ? pl : pp;
+      const uint32_t (&ds)[2][2] = part ? dl : dd;
+      pt[part][0] = movmatrix_t(ps[0][0]);
+      pt[part][1] = movmatrix_t(ps[1][0]);
+      pt[part][2] = movmatrix_t(ps[0][1]);
+      pt[part][3] = movmatrix_t(ps[1][1]);
+      dt[part][0] = movmatrix_t(ds[0][0]);
+      dt[part][1] = movmatrix_t(ds[1][0]);
+      dt[part][2] = movmatrix_t(ds[0][1]);
+      dt[part][3] = movmatrix_t(ds[1][1]);
+    }
     // The step's K/V stage is free now (S, dP and dQ are done).  Each 16-key
     // fp32 tile (dV, then dK) is written into it in fragment order: tile row m
     // (token m >> 2 of slot m & 3) at (m & 3) * POOL_PITCH + (m >> 2) * RED_ROW,
@@ -375,15 +386,15 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
 #pragma unroll
       for (int which = 0; which < 2; ++which) {   // 0: dV = P^T dO, 1: dK = (scale dS)^T Q
         const uint32_t bsrc = which ? qs : dos;
-        const uint32_t a0 = which ? dt0 : pt0, a1 = which ? dt1 : pt1;
-        const uint32_t a2 = which ? dt2 : pt2, a3 = which ? dt3 : pt3;
+        const uint32_t (&ah)[4] = which ? dt[0] : pt[0];
+        const uint32_t (&alo)[4] = which ? dt[1] : pt[1];
         if (which == 1) {
           // the dV tile's reductions must have read it before dK overwrites it
           bulk_wait_read0_if(lane < 4);
           __syncwarp();
         }
-        // two 16-column blocks per iteration: four independent MMAs before
-        // their results are stored
+        // two 16-column blocks per iteration: four independent accumulators
+        // (each takes the hi and then the lo part) before their results are stored
 #pragma unroll
         for (int j = 0; j < D / 16; j += 2) {
           uint32_t b[2][4];
@@ -399,8 +410,13 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) c2[u][h][e] = 0.f;
-              mma_f16_16816(c2[u][h], a0, a1, a2, a3, b[u][2 * h], b[u][2 * h + 1]);
+              mma_bf16_16816(c2[u][h], ah[0], ah[1], ah[2], ah[3], b[u][2 * h], b[u][2 * h + 1]);
             }
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              mma_bf16_16816(c2[u][h], alo[0], alo[1], alo[2], alo[3], b[u][2 * h], b[u][2 * h + 1]);
 #pragma unroll
           for (int u = 0; u < 2; ++u)
 #pragma unroll

@@ -59,6 +59,27 @@ def test_bounded_wait_gives_up_and_stream_survives():
     dsa.check_device_error()
 
 
+# ---------------------------------------------------------------- traffic probe
+@pytest.mark.parametrize("d", [64, 128])
+def test_probe_traffic_does_its_reductions(d):
+    """The traffic replay behind the attention kernels' roofline does the work
+    it claims: every step adds 4 pools x 4 rows x d values into each of dK and
+    dV, so their sums grow by exactly that count times the added value."""
+    L, steps = 4096, 5000
+    k = torch.randn(L, d, device=DEV).to(torch.bfloat16)
+    v = torch.randn(L, d, device=DEV).to(torch.bfloat16)
+    dk = torch.zeros(L, d, device=DEV)
+    dv = torch.zeros(L, d, device=DEV)
+    dsa.probe_traffic(d, L, k, v, None, None, steps, seed=3)
+    dsa.probe_traffic(d, L, k, v, dk, dv, steps, seed=4)
+    dsa.check_device_error()
+    want = steps * 16 * d * 1e-30
+    for t in (dk, dv):
+        got = float(t.double().sum())
+        assert abs(got - want) <= 1e-3 * want, (got, want)
+        assert int((t != 0).any(1).sum()) > L // 2     # the pools are spread over the table
+
+
 # ---------------------------------------------------------------- pool keys
 @pytest.mark.parametrize("dtype,di", [("bf16", 64), ("bf16", 128), ("fp32", 64), ("fp32", 128)])
 def test_pool_keys_bitexact(dtype, di):
@@ -234,6 +255,53 @@ def test_attn_bwd_matches_oracle(Hq, d, k, use_o_acc):
     errs = {name: float(np.abs(got.cpu().numpy() - ref).max())
             for name, got, ref in (("dQ", dq, dQr), ("dK", dk, dKr), ("dV", dv, dVr))}
     assert max(errs.values()) <= 2e-2, errs
+
+
+@pytest.mark.parametrize("case", ["dO_times_1e-6", "beyond_fp16_range", "unit_scale"])
+@pytest.mark.parametrize("use_o_acc", [False, True])
+def test_attn_bwd_scaled_inputs(case, use_o_acc):
+    """Inputs far from unit scale, compared element by element with the oracle.
+
+    A loss-scaled upstream gradient (dO ~ 1e-6 per element) and Q / dO entries
+    above 65504 (fp16's largest finite value, with K scaled down by the same
+    power of two so the softmax stays unsaturated) are legal bf16 inputs.  The
+    gradients scale with the inputs: dV with dO, dK with dO * Q, dQ with dO * K,
+    so each is held to the 2e-2 bound times its own scale."""
+    L, Hq, d, k = 1000, 16, 128, 32
+    Q, K, V, dO, idx = _attn_case(L, Hq, d, k, "bf16", seed=31)
+    sQ = sK = sdO = 1.0
+    if case == "dO_times_1e-6":
+        sdO = 1e-6
+    elif case == "beyond_fp16_range":
+        sQ, sK, sdO = 2.0 ** 17, 2.0 ** -17, 2.0 ** 17
+    Q = (Q.float() * sQ).to(torch.bfloat16)
+    K = (K.float() * sK).to(torch.bfloat16)
+    dO = (dO.float() * sdO).to(torch.bfloat16)
+    if case == "beyond_fp16_range":
+        assert float(Q.float().abs().max()) > 65504 and float(dO.float().abs().max()) > 65504
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale)
+    dev = [t.to(DEV) for t in (Q, K, V, dO)]
+    idx_d = torch.from_numpy(idx).to(DEV)
+    O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    o_acc = torch.empty((L, Hq, d), device=DEV) if use_o_acc else None
+    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, o_acc=o_acc)
+    dq = torch.empty((L, Hq, d), device=DEV)
+    dk = torch.empty((L, d), device=DEV)
+    dv = torch.empty((L, d), device=DEV)
+    ws = None if use_o_acc else dsa.alloc_backward_workspace(dims, DEV)
+    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws, o_acc=o_acc)
+    dsa.check_device_error()
+    dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
+    grad_scale = {"dQ": sdO * sK, "dK": sdO * sQ, "dV": sdO}
+    for name, got, ref in (("dQ", dq, dQr), ("dK", dk, dKr), ("dV", dv, dVr)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(g)), name
+        err = float(np.abs(g - ref).max()) / grad_scale[name]
+        assert err <= 2e-2, (name, err)
+        # not flushed to zero: the gradient carries the reference's magnitude
+        assert np.abs(g).max() >= 0.5 * np.abs(ref).max(), name
 
 
 def test_attn_bad_index_is_skipped_and_reported():
