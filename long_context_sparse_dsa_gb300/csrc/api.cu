@@ -155,6 +155,28 @@ namespace dsa {
 // Lets entry points defined in other files of the library report a detail
 // through dsa_last_error_message.
 void set_last_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
+// The checks dsa_layer_fwd makes on its dims and tensor pointers (everything
+// but the workspace and o_acc), for entry points in other files that must
+// reject bad arguments before they enqueue anything.
+dsa_status check_layer_fwd_args(const dsa_dims* dims, const void* q, const void* k, const void* v,
+                                const void* q_idx, const void* k_idx, const float* w, const void* o,
+                                const float* lse, const int32_t* idx, const void* kpool) {
+  g_msg[0] = 0;
+  dsa_status st = check_dims(dims, false);
+  if (st) return st;
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(k);
+  REQUIRE_PTR(v);
+  REQUIRE_PTR(q_idx);
+  REQUIRE_PTR(k_idx);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(o);
+  REQUIRE_PTR(lse);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(kpool);
+  return DSA_OK;
+}
 }  // namespace dsa
 
 extern "C" {
@@ -272,19 +294,8 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* 
 dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, const void* v, const void* q_idx,
                          const void* k_idx, const float* w, void* o, float* lse, float* o_acc, int32_t* idx,
                          void* kpool, void* ws, size_t ws_bytes, dsa_stream_t stream) {
-  g_msg[0] = 0;
-  dsa_status st = check_dims(dims, false);
+  dsa_status st = dsa::check_layer_fwd_args(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool);
   if (st) return st;
-  REQUIRE_PTR(q);
-  REQUIRE_PTR(k);
-  REQUIRE_PTR(v);
-  REQUIRE_PTR(q_idx);
-  REQUIRE_PTR(k_idx);
-  REQUIRE_PTR(w);
-  REQUIRE_PTR(o);
-  REQUIRE_PTR(lse);
-  REQUIRE_PTR(idx);
-  REQUIRE_PTR(kpool);
   if (o_acc != nullptr && !aligned16(o_acc)) return fail(DSA_ERR_INVALID_ARG, "o_acc is not 16-byte aligned");
   const size_t need = dsa_workspace_bytes(dims);
   if (ws == nullptr || ws_bytes < need)

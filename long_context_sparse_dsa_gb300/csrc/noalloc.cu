@@ -19,6 +19,9 @@
 
 namespace dsa {
 void set_last_error_message(const char* msg);  // defined in api.cu
+dsa_status check_layer_fwd_args(const dsa_dims* dims, const void* q, const void* k, const void* v,
+                                const void* q_idx, const void* k_idx, const float* w, const void* o,
+                                const float* lse, const int32_t* idx, const void* kpool);  // api.cu
 }
 
 namespace {
@@ -62,7 +65,9 @@ dsa_status scratch_address(float** out) {
 extern "C" dsa_status dsa_layer_fwd_noalloc(const dsa_dims* dims, const void* q, const void* k, const void* v,
                                             const void* q_idx, const void* k_idx, const float* w, void* o,
                                             float* lse, int32_t* idx, void* kpool, dsa_stream_t stream) {
-  dsa_status st = dsa_validate_dims(dims, 0);
+  // every argument is checked before anything is enqueued (or the scratch
+  // array's address is looked up)
+  dsa_status st = dsa::check_layer_fwd_args(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool);
   if (st != DSA_OK) return st;
   const int64_t P = dims->L / 4;
   const int64_t rows_fit = (int64_t)(kNoallocScratchBytes / sizeof(float)) / P;

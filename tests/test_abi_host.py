@@ -107,6 +107,34 @@ def test_null_and_misaligned_pointers_fail_before_launch(lib):
     assert lib.dsa_selftest_bounded_wait(0, None) == dsa.DSA_ERR_INVALID_ARG
 
 
+def test_noalloc_checks_every_pointer_before_anything_is_enqueued(lib):
+    """dsa_layer_fwd_noalloc rejects a NULL or misaligned tensor pointer with
+    DSA_ERR_INVALID_ARG before it touches the GPU: on a host without a GPU any
+    CUDA call it made first (the scratch array's address, a launch) would
+    report DSA_ERR_CUDA instead."""
+    d = _dims()
+    p = ctypes.c_void_p(256)
+    names = ["q", "k", "v", "q_idx", "k_idx", "w", "o", "lse", "idx", "kpool"]
+    for i, name in enumerate(names):
+        for bad in (None, ctypes.c_void_p(264)):
+            args = [p] * len(names)
+            args[i] = bad
+            assert lib.dsa_layer_fwd_noalloc(ctypes.byref(d), *args, None) == dsa.DSA_ERR_INVALID_ARG, name
+            assert name.encode() in lib.dsa_last_error_message()
+
+
+def test_probe_validates_before_launch(lib):
+    p, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)
+    f = lib.dsa_probe_traffic
+    assert f(96, 4096, p, p, None, None, 10, 0, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(128, 4094, p, p, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(128, 4096, p, p, None, None, 0, 0, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(128, 4096, None, p, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(128, 4096, p, odd, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(128, 4096, p, p, p, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG      # only one of dk/dv
+    assert f(128, 4096, p, p, p, odd, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
+
+
 def test_binding_has_no_cpu_path():
     import inspect
     src = inspect.getsource(dsa)
