@@ -54,19 +54,12 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# attention kernels from one ncu capture at the full 128k workload (summary and
-# command in profiles/dram_traffic_attention_128k.md).  A figure is reported
-# only while the kernel's source files hash as they did when it was captured;
-# after any change to them the bench reports null until it is captured again.
-TRAFFIC = {
-    ("bf16_128k_needle", "attn_bwd"): {"bytes": 11048906752 + 8431785472,
-                                       "sources": {"attn_bwd.cu": "bac6e9f136e06ee9", "gather.cuh": "9c5588b13d0916cd",
-                                                   "common.cuh": "ccd81ae7439639d8"}},
-    ("bf16_128k_needle", "attn_fwd"): {"bytes": 1273865728 + 1568081664,
-                                       "sources": {"attn_fwd.cu": "ffdff854d43dc7cb", "gather.cuh": "9c5588b13d0916cd",
-                                                   "common.cuh": "ccd81ae7439639d8"}},
-}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the bench at the full 128k workload (one-pass metrics).  A
+# figure is reported only while the kernel's source files hash as they did
+# when it was captured; after any change to them the bench reports null until
+# it is captured again.
+TRAFFIC = {}
 
 
 def measured_traffic(workload: str, kernel: str):
@@ -159,10 +152,12 @@ def algorithmic(wl):
         "topk": {"bytes": 4.0 * pairs + 4.0 * L * k},
         # gathered K and V rows; Q read, O written, idx read, LSE written
         "attn_fwd": {"bytes": nkeys * 2 * d * eb + L * Hq * d * eb * 2 + L * k * 4 + L * Hq * 4 + acc,
-                     "flops": (6.0 if acc else 4.0) * Hq * d * nkeys},
+                     "l2_bytes": nkeys * 2 * d * eb,
+                     "flops": 4.0 * Hq * d * nkeys},
         # gathered K and V rows, fp32 dK and dV reductions; Q, dO, o_acc read, dQ written; idx, LSE read
         "attn_bwd": {"bytes": nkeys * 2 * d * eb + nkeys * 2 * d * 4 + L * Hq * d * (2 * eb + 4) + acc
                      + L * k * 4 + L * Hq * 4,
+                     "l2_bytes": nkeys * 2 * d * eb + nkeys * 2 * d * 4,
                      "flops": 10.0 * Hq * d * nkeys},
         "nkeys": nkeys, "pairs": pairs,
     }
@@ -285,10 +280,11 @@ def run_ours(args, rank, world):
     launch_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
     alg = algorithmic(wl)
     peaks, peak_kind = load_peaks()
+    ceilings = l2_ceilings(dsa, wl, d_in["K"], d_in["V"], stream, dev, with_bwd)
     dominant = max(k_ms, key=k_ms.get)
-    rl = roofline(dominant, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))
+    rl = roofline(dominant, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks), ceilings)
     kernels = {nm: {"ms_per_step": round(k_ms[nm], 4), "launches_per_step": len(per_kernel[nm]) // steps,
-                    **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks))} for nm in k_ms}
+                    **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks), ceilings)} for nm in k_ms}
 
     # device memory of the layer: every buffer is a torch allocation (the library allocates nothing)
     flush_bytes = flush.numel()
@@ -320,15 +316,44 @@ def run_ours(args, rank, world):
     }
 
 
-def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks):
+def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks, ceilings=None):
+    """Roofline of one kernel from its mean CUDA-event launch time.
+
+    The indexer is a tensor-core contraction (burst bf16 peak); top-k and the
+    pool keys stream from HBM (measured copy bandwidth).  The attention kernels
+    gather K/V rows from a table that stays in L2 and the backward adds fp32
+    dK/dV rows into one: their bound is L2 traffic, so they are measured
+    against a ceiling taken in the same run -- a replay of the same gathers and
+    bulk reductions with no arithmetic (dsa_probe_traffic) -- with the HBM and
+    tensor-core fractions beside it."""
     ms = launch_ms[nm]
     hbm = peaks["hbm_gbs"]
+    traffic = measured_traffic(wl.name, nm)
     if nm == "indexer":
         flops = alg["indexer"]["flops"] / nchunks      # one launch = one chunk (average)
         a = flops / (ms * 1e-3) / 1e12
         pk = peaks["bf16_tflops"]
-        return {"bound": "tensor", "achieved": round(a, 2), "peak": pk, "unit": "TFLOP/s", "frac": round(a / pk, 4),
-                "traffic": None, "peak_source": f"{peak_kind} bf16 dense (burst)"}
+        out = {"bound": "tensor", "achieved": round(a, 2), "peak": pk, "unit": "TFLOP/s", "frac": round(a / pk, 4),
+               "traffic": traffic, "peak_source": f"{peak_kind} bf16 dense (burst)"}
+        if traffic is not None:
+            out["hbm_frac"] = round(traffic / (ms * 1e-3) / 1e9 / hbm, 4)
+        return out
+    if nm in ("attn_fwd", "attn_bwd") and ceilings and nm in ceilings:
+        c = ceilings[nm]
+        b = alg[nm]["l2_bytes"]
+        a = b / (ms * 1e-3) / 1e9
+        fl = alg[nm]["flops"] / (ms * 1e-3) / 1e12
+        tpk = peaks["bf16_tflops_sustained"]
+        out = {"bound": "l2", "achieved": round(a, 1), "peak": round(c["gbs"], 1), "unit": "GB/s",
+               "frac": round(a / c["gbs"], 4), "traffic": traffic,
+               "peak_source": c["what"],
+               "tensor": {"achieved_tflops": round(fl, 2), "peak": tpk, "frac": round(fl / tpk, 4),
+                          "peak_source": f"{peak_kind} bf16 dense (sustained)"}}
+        if traffic is not None:
+            out["hbm"] = {"achieved_gbs": round(traffic / (ms * 1e-3) / 1e9, 1), "peak": hbm,
+                          "frac": round(traffic / (ms * 1e-3) / 1e9 / hbm, 4),
+                          "peak_source": f"{peak_kind} HBM copy"}
+        return out
     if nm == "topk":
         b = alg["topk"]["bytes"] / nchunks
     elif nm == "pool_keys":
@@ -337,7 +362,43 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks):
         b = alg[nm]["bytes"]
     a = b / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
-            "traffic": measured_traffic(wl.name, nm), "peak_source": f"{peak_kind} HBM copy"}
+            "traffic": traffic, "peak_source": f"{peak_kind} HBM copy"}
+
+
+def l2_ceilings(dsa, wl, k, v, stream, dev, with_bwd, reps=3):
+    """Same-run ceilings for the attention kernels: dsa_probe_traffic replays
+    the steps of the layer (L x ceil((k+1)/4) steps of 16 keys, the step count
+    the attention kernels run) with the same gathers (and, for the backward,
+    the same fp32 bulk reductions) and no arithmetic.  Best of `reps`."""
+    steps = wl.L * ((wl.k + 1 + 3) // 4)
+    gather_b = steps * 16 * 2 * wl.d * 2
+    red_b = steps * 16 * 2 * wl.d * 4
+    out = {}
+    scratch = None
+    if with_bwd:
+        scratch = (torch.zeros((wl.L, wl.d), device=dev), torch.zeros((wl.L, wl.d), device=dev))
+    for nm, red in (("attn_fwd", False), ("attn_bwd", True)):
+        if red and not with_bwd:
+            continue
+        dk, dv = scratch if red else (None, None)
+        best = None
+        for r in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dsa.probe_traffic(wl.d, wl.L, k, v, dk, dv, steps, seed=11 + r, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            if r > 0:
+                best = ms if best is None else min(best, ms)
+        b = gather_b + (red_b if red else 0)
+        what = (f"same-run replay of this kernel's {steps} 16-key steps with no arithmetic (dsa_probe_traffic): "
+                f"16-byte cp.async gathers of 4 random whole pools of K and V per step"
+                + (", then one fp32 bulk reduction per pool into each of dK and dV" if red else "")
+                + f"; best of {reps}: {best:.3f} ms for {b / 1e9:.1f} GB")
+        out[nm] = {"gbs": b / (best * 1e-3) / 1e9, "ms": best, "bytes": b, "what": what}
+    dsa.check_device_error(stream)
+    return out
 
 
 def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev):
@@ -348,14 +409,14 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     Consecutive steps are pipelined over three streams with two device buffer
     sets: the inputs of step i+1 go in and the outputs of step i-1 come back
     while step i runs, and each step's copies still precede and follow its own
-    layer.  Measured back to back on one box at 128k: 67.3 ms per step
-    pipelined, 79.5 ms with every copy serialised on one stream.  If the
+    layer.  --e2e-steps steps (10 by default) are timed, pipeline fill and drain included, and
+    the box's measured copy rates are reported beside the figure.  If the
     pipelined run raises, the serialised run is reported and "mode" says why."""
     names = list(d_in.keys())
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
     d2h = sum(t.numel() * t.element_size() for t in outs)
-    steps = max(1, min(args.steps, 5))
+    steps = max(1, args.e2e_steps)
 
     def layer(d, o, lse, grads, s):
         dsa.layer_fwd(dims, d["Q"], d["K"], d["V"], d["q_I"], d["k_I"], d["w"], o, lse, bufs.idx, bufs.kpool,
@@ -373,7 +434,36 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
         mode = f"serialised on one stream (pipelined run raised {type(exc).__name__}: {exc})"[:240]
     value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
     return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "mode": mode}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3), "mode": mode,
+            "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev)}
+
+
+def copy_bandwidth(host, names, d_in, outs, stream, dev):
+    """The host<->device copy rates this box gives the end-to-end leg: the
+    step's input copies from pinned memory alone, then its output copies to
+    pinned memory alone, each timed with CUDA events on one stream (best of 3)."""
+    pinned = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d_b = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h_b = sum(t.numel() * t.element_size() for t in outs)
+
+    def timed(fn):
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    ms_in = timed(lambda: [d_in[n].copy_(host[n], non_blocking=True) for n in names])
+    ms_out = timed(lambda: [dst.copy_(src, non_blocking=True) for src, dst in zip(outs, pinned)])
+    return {"h2d_gbs": round(h2d_b / (ms_in * 1e-3) / 1e9, 1), "h2d_ms": round(ms_in, 3),
+            "d2h_gbs": round(d2h_b / (ms_out * 1e-3) / 1e9, 1), "d2h_ms": round(ms_out, 3)}
 
 
 def _e2e_pipelined(host, names, d_in, outs, layer, steps, dev):
@@ -500,9 +590,27 @@ def oracle_sample(wl, n_rows: int, seed: int = 7):
     t_rows = time.perf_counter() - t1
     # the pool-key pass is per layer: charge it in proportion to the rows sampled
     secs = t_rows + t_pool * (n_rows / wl.L)
-    desc = (f"{n_rows} query rows drawn uniformly from the second half of the sequence: indexer scores over all "
-            f"eligible pools, top-{wl.k}, attention {wl.passes} with dK/dV; pool keys once, charged per row")
+    desc = (f"extrapolated from {n_rows} sampled query rows (drawn uniformly from the second half of the "
+            f"sequence): indexer scores over all eligible pools, top-{wl.k}, attention {wl.passes} with dK/dV; "
+            f"pool keys once, charged per row; tokens/s = rows / their single-core time")
     return secs, n_rows, desc
+
+
+def oracle_full_tiny():
+    """The oracle's whole forward on the smallest workload (L=4096, fp32),
+    single-threaded, every row: a measured (not extrapolated) CPU time."""
+    import oracle
+
+    oracle.build()
+    wl = dsa_inputs.WORKLOADS["tiny_fp32_fwd"]
+    host = dsa_inputs.make(wl, ("Q", "K", "V", "q_I", "k_I", "w"))
+    f = {n: host[n].to(torch.float32).numpy() for n in host}
+    t0 = time.perf_counter()
+    oracle.layer_fwd(f["Q"], f["K"], f["V"], f["q_I"], f["k_I"], f["w"], wl.k, wl.scale, False)
+    secs = time.perf_counter() - t0
+    return {"workload": wl.name, "L": wl.L, "pass": wl.passes, "seconds": round(secs, 3),
+            "value": round(wl.L / secs, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "every row of the workload (measured, not extrapolated)"}
 
 
 def run_reference(args):
@@ -538,6 +646,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per reference step")
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10, help="end-to-end steps (at least 1; 10 by default)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -554,7 +663,8 @@ def main():
             wl = dsa_inputs.WORKLOADS[args.workload]
             secs, n, desc = oracle_sample(wl, args.cpu_rows)
             line["cpu_baseline"] = {"value": round(n / secs, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                    "sample": desc, "seconds": round(secs, 2), **host_cpu()}
+                                    "sample": desc, "seconds": round(secs, 2), "extrapolated": True,
+                                    **host_cpu(), "full_run_tiny_fwd": oracle_full_tiny()}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -9,7 +9,8 @@ or no GPU is present, calls raise.
 Entry points (same names as the C ABI, without the ``dsa_`` prefix):
 pool_keys, indexer_score, topk, sparse_attn_fwd, sparse_attn_bwd,
 layer_fwd, layer_bwd, check_device_error, workspace_bytes, bwd_workspace_bytes,
-validate_dims, layer_fwd_noalloc.
+validate_dims, layer_fwd_noalloc; and the measurement probe probe_traffic
+(``include/dsa_probe.h``).
 """
 from __future__ import annotations
 
@@ -20,7 +21,8 @@ from dataclasses import dataclass
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
-HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "dsa.h")
+INCLUDE_DIR = os.path.join(os.path.dirname(_HERE), "include")
+HEADER_PATH = os.path.join(INCLUDE_DIR, "dsa.h")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
 DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_BAD_INDEX = 4, 5, 6
@@ -74,6 +76,7 @@ def _load():
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
             "dsa_selftest_bounded_wait": ([u32, P], ctypes.c_int),
+            "dsa_probe_traffic": ([i32, i64, P, P, P, P, i64, ctypes.c_uint64, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -89,10 +92,14 @@ def library():
 
 
 def header_functions():
-    """Names of the functions ``include/dsa.h`` declares."""
-    src = open(HEADER_PATH).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", src)))
+    """Names of the functions the headers under ``include/`` declare."""
+    names = set()
+    for fn in sorted(os.listdir(INCLUDE_DIR)):
+        if fn.endswith(".h"):
+            src = open(os.path.join(INCLUDE_DIR, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
 
 
 def status_string(status: int) -> str:
@@ -190,6 +197,12 @@ def layer_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_bytes=No
 
 def check_device_error(stream=None):
     _check(_load().dsa_check_device_error(_stream(stream)), "dsa_check_device_error")
+
+
+def probe_traffic(d, L, k, v, dk, dv, steps, seed=0, stream=None):
+    """Replay the attention kernels' L2 traffic with no arithmetic (include/dsa_probe.h)."""
+    _check(_load().dsa_probe_traffic(int(d), int(L), _ptr(k), _ptr(v), _ptr(dk), _ptr(dv), int(steps), int(seed),
+                                     _stream(stream)), "dsa_probe_traffic")
 
 
 def set_wait_limit(spins: int):

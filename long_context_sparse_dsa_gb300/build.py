@@ -38,8 +38,8 @@ def _sources():
 
 def _digest() -> str:
     h = hashlib.sha256()
-    for f in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + [
-            os.path.join(INCLUDE, "dsa.h")]:
+    for f in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + sorted(
+            glob.glob(os.path.join(INCLUDE, "*.h"))):
         h.update(f.encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
