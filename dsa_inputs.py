@@ -57,7 +57,10 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
     def integer_twin(self) -> "Workload":
-        """Same shapes, indexer inputs drawn as small integers so fp32 scores are exact."""
+        """Same shapes, indexer inputs drawn as small integers so fp32 scores are exact.
+
+        With a needle, the twin's indexer needle is an integer vector as well
+        (see make()), so the heavy-tailed selection structure is kept."""
         return self.with_(name=self.name + "_int", indexer="int3", weights="int1_4")
 
 
@@ -131,17 +134,23 @@ def make(wl: Workload, tensors=("Q", "K", "V", "q_I", "k_I", "w", "dO"), pin: bo
     Q [L,Hq,d], K [L,d], V [L,d], dO [L,Hq,d] and q_I [L,Hi,di], k_I [L,di] in
     the layer dtype; w [L,Hi] fp32.  With a needle fraction, every needle
     token gets 4*sqrt(width)*u added (before the cast) to Q (all heads), K,
-    q_I (all heads) and k_I, with one shared unit vector u per width.
+    q_I (all heads) and k_I, with one shared unit vector u per width.  When
+    the indexer inputs are integers (an integer twin), the indexer's needle
+    is the integer vector 3*sign(u) instead, so q_I and k_I stay integers
+    (|q_I| <= 6, |kpool| <= 24) and every fp32 score stays exact.
     """
     dt = _torch_dtype(wl)
     mask = u_att = u_idx = None
     if wl.needle > 0:
         mask, u_att, u_idx = needle_plan(wl)
 
-    def needle_add(u, width):
+    def needle_add(u, width, integer=False):
         if mask is None:
             return None
         amp = 4.0 * math.sqrt(width)
+        if integer:
+            u = 3.0 * torch.sign(u)
+            amp = 1.0
 
         def add(r0, blk):
             m = mask[r0:r0 + blk.shape[0]]
@@ -163,9 +172,10 @@ def make(wl: Workload, tensors=("Q", "K", "V", "q_I", "k_I", "w", "dO"), pin: bo
         elif name == "dO":
             out[name] = _draw((wl.L, wl.Hq, wl.d), "normal", g, dt, None, pin)
         elif name == "q_I":
-            out[name] = _draw((wl.L, wl.Hi, wl.di), wl.indexer, g, dt, needle_add(u_idx, wl.di), pin)
+            out[name] = _draw((wl.L, wl.Hi, wl.di), wl.indexer, g, dt,
+                              needle_add(u_idx, wl.di, wl.indexer != "normal"), pin)
         elif name == "k_I":
-            out[name] = _draw((wl.L, wl.di), wl.indexer, g, dt, needle_add(u_idx, wl.di), pin)
+            out[name] = _draw((wl.L, wl.di), wl.indexer, g, dt, needle_add(u_idx, wl.di, wl.indexer != "normal"), pin)
         elif name == "w":
             out[name] = _draw((wl.L, wl.Hi), wl.weights, g, torch.float32, None, pin)
         else:
