@@ -6,9 +6,9 @@ heads sharing one K/V head of d=128, an indexer of 8 heads x 64, 32768 pools
 of 4 tokens, top-512 pools per query, indexer chunks of 8192 queries.
 Synthetic seeded inputs (dsa_inputs.py); no dataset, no trained weights.
 
-One step = the whole layer: pool keys, for each 8192-query chunk the indexer
-scores and the top-k, sparse attention forward, then the backward (dQ, dK,
-dV).  It calls the C-ABI entry points one by one on one stream, with CUDA
+One step = the whole layer: pool keys, for each 8192-query chunk the fused
+indexer scores + top-k selection, sparse attention forward, then the backward
+(dQ, dK, dV).  It calls the C-ABI entry points one by one on one stream, with CUDA
 events between them, so the per-kernel durations (and the roofline of the
 dominant kernel) are measured live in the same run.
 
@@ -208,10 +208,14 @@ def run_ours(args, rank, world):
     bws = None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
     stream = torch.cuda.current_stream(dev)
-    scores = bufs.ws.view(torch.float32)
     C = wl.q_chunk
     chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
-    launches_per_step = 1 + 2 * len(chunks) + 1 + (1 if with_bwd else 0)
+    # kernels per step: pool keys; per chunk the fused indexer + top-k (sampled
+    # scores when the chunk has rows of more than 2048 pools, thresholds,
+    # candidates, selection, fallback scores, fallback top-k; fp32 layers: the
+    # indexer and the top-k); the forward; the backward
+    per_chunk = [(5 + (((q0 + n) >> 2) > 2048)) if wl.dtype == "bf16" else 2 for q0, n in chunks]
+    launches_per_step = 1 + sum(per_chunk) + 1 + (1 if with_bwd else 0)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -226,13 +230,9 @@ def run_ours(args, rank, world):
             marks.append(("pool_keys", timers.pop()))
             marks[-1][1].record(stream)
         for q0, n in chunks:
-            dsa.indexer_score(dims, d_in["q_I"], bufs.kpool, d_in["w"], q0, n, scores, stream)
+            dsa.indexer_topk(dims, d_in["q_I"], bufs.kpool, d_in["w"], q0, n, bufs.idx, bufs.ws, stream=stream)
             if timers is not None:
-                marks.append(("indexer", timers.pop()))
-                marks[-1][1].record(stream)
-            dsa.topk(dims, scores, q0, n, bufs.idx, stream)
-            if timers is not None:
-                marks.append(("topk", timers.pop()))
+                marks.append(("indexer_topk", timers.pop()))
                 marks[-1][1].record(stream)
         dsa.sparse_attn_fwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, stream,
                             o_acc=bufs.o_acc)
@@ -254,7 +254,7 @@ def run_ours(args, rank, world):
 
     per_kernel = {}
     step_ms = []
-    n_marks = 2 + 2 * len(chunks) + 2 + 1
+    n_marks = 2 + len(chunks) + 2 + 1
     with ClockSampler(local) as clk:
         if world > 1:
             torch.distributed.barrier()
@@ -280,17 +280,17 @@ def run_ours(args, rank, world):
     launch_ms = {nm: sum(v) / len(v) for nm, v in per_kernel.items()}
     alg = algorithmic(wl)
     peaks, peak_kind = load_peaks()
-    ceilings = l2_ceilings(dsa, wl, d_in["K"], d_in["V"], stream, dev, with_bwd)
+    ceilings = l2_ceilings(dsa, dims, wl, d_in["K"], d_in["V"], bufs.idx, stream, dev, with_bwd)
     dominant = max(k_ms, key=k_ms.get)
     rl = roofline(dominant, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks), ceilings)
-    kernels = {nm: {"ms_per_step": round(k_ms[nm], 4), "launches_per_step": len(per_kernel[nm]) // steps,
+    kernels = {nm: {"ms_per_step": round(k_ms[nm], 4), "calls_per_step": len(per_kernel[nm]) // steps,
                     **roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, len(chunks), ceilings)} for nm in k_ms}
 
     # device memory of the layer: every buffer is a torch allocation (the library allocates nothing)
     flush_bytes = flush.numel()
     peak = torch.cuda.max_memory_allocated(dev)
     memory = {"peak_allocated_gib": round((peak - flush_bytes) / 2**30, 3),
-              "score_workspace_gib": round(bufs.ws.numel() / 2**30, 3),
+              "indexer_topk_workspace_gib": round(bufs.ws.numel() / 2**30, 3),
               "what": "torch.cuda.max_memory_allocated over inputs, outputs and workspaces, less the 256 MiB "
                       "L2-flush buffer; the library allocates no device memory"}
 
@@ -329,8 +329,10 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks, ceilings=N
     ms = launch_ms[nm]
     hbm = peaks["hbm_gbs"]
     traffic = measured_traffic(wl.name, nm)
-    if nm == "indexer":
-        flops = alg["indexer"]["flops"] / nchunks      # one launch = one chunk (average)
+    if nm in ("indexer", "indexer_topk"):
+        # one call = one chunk (average); the work counted is the indexer's
+        # causal flops (the sampled pass and the selection are overhead)
+        flops = alg["indexer"]["flops"] / nchunks
         a = flops / (ms * 1e-3) / 1e12
         pk = peaks["bf16_tflops"]
         out = {"bound": "tensor", "achieved": round(a, 2), "peak": pk, "unit": "TFLOP/s", "frac": round(a / pk, 4),
@@ -365,14 +367,13 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks, ceilings=N
             "traffic": traffic, "peak_source": f"{peak_kind} HBM copy"}
 
 
-def l2_ceilings(dsa, wl, k, v, stream, dev, with_bwd, reps=3):
+def l2_ceilings(dsa, dims, wl, k, v, idx, stream, dev, with_bwd, reps=3):
     """Same-run ceilings for the attention kernels: dsa_probe_traffic replays
-    the steps of the layer (L x ceil((k+1)/4) steps of 16 keys, the step count
-    the attention kernels run) with the same gathers (and, for the backward,
-    the same fp32 bulk reductions) and no arithmetic.  Best of `reps`."""
-    steps = wl.L * ((wl.k + 1 + 3) // 4)
-    gather_b = steps * 16 * 2 * wl.d * 2
-    red_b = steps * 16 * 2 * wl.d * 4
+    the kernels' own steps over the layer's own selection (the same pool
+    gathers and, for the backward, the same fp32 bulk reductions, with the
+    same occupancy) and does no arithmetic.  Best of `reps`; the bytes are the
+    kernels' logical L2 bytes, so ceiling / achieved = kernel time / replay time."""
+    alg = algorithmic(wl)
     out = {}
     scratch = None
     if with_bwd:
@@ -385,17 +386,17 @@ def l2_ceilings(dsa, wl, k, v, stream, dev, with_bwd, reps=3):
         for r in range(reps + 1):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            dsa.probe_traffic(wl.d, wl.L, k, v, dk, dv, steps, seed=11 + r, stream=stream)
+            dsa.probe_traffic(dims, k, v, idx, dk, dv, stream=stream)
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1)
             if r > 0:
                 best = ms if best is None else min(best, ms)
-        b = gather_b + (red_b if red else 0)
-        what = (f"same-run replay of this kernel's {steps} 16-key steps with no arithmetic (dsa_probe_traffic): "
-                f"16-byte cp.async gathers of 4 random whole pools of K and V per step"
-                + (", then one fp32 bulk reduction per pool into each of dK and dV" if red else "")
-                + f"; best of {reps}: {best:.3f} ms for {b / 1e9:.1f} GB")
+        b = alg[nm]["l2_bytes"]
+        what = ("same-run replay of this kernel's steps over the layer's own selection, no arithmetic "
+                "(dsa_probe_traffic): the same 16-byte cp.async pool gathers of K and V"
+                + (" and one fp32 bulk reduction per pool slot into each of dK and dV" if red else "")
+                + f", same occupancy; best of {reps}: {best:.3f} ms for {b / 1e9:.1f} GB")
         out[nm] = {"gbs": b / (best * 1e-3) / 1e9, "ms": best, "bytes": b, "what": what}
     dsa.check_device_error(stream)
     return out

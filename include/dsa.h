@@ -112,10 +112,19 @@ const char *dsa_last_error_message(void);
  * DSA_ERR_UNSUPPORTED. */
 dsa_status dsa_validate_dims(const dsa_dims *dims, int32_t with_backward);
 
-/* Bytes of device workspace dsa_layer_fwd needs: the fp32 score block of one
- * query chunk, q_chunk * (L/4) * 4 bytes, rounded up to 256.  Returns 0 if
- * dims are invalid. */
+/* Bytes of device workspace dsa_layer_fwd needs: that of dsa_indexer_topk
+ * for one query chunk, dsa_indexer_topk_workspace_bytes(dims,
+ * min(q_chunk, L)).  Returns 0 if dims are invalid. */
 size_t dsa_workspace_bytes(const dsa_dims *dims);
+
+/* Bytes of device workspace dsa_indexer_topk needs for q_count queries.
+ * fp32 layers: the fp32 score block, q_count * (L/4) * 4 bytes.  bf16 layers:
+ * the score rows of the fallback (q_count * (L/4) * 4 bytes), a sampled score
+ * block (1/32 of that), the candidate lists (q_count * S * 8 bytes, with
+ * S = max(4096, 64 * ceil(L/8192))), their lengths (q_count * ceil(L/8192) *
+ * 16 bytes) and a few per-row words, each part rounded up to 256.  Returns 0
+ * if dims are invalid or q_count is outside 1 .. L. */
+size_t dsa_indexer_topk_workspace_bytes(const dsa_dims *dims, int64_t q_count);
 
 /* Bytes of device workspace dsa_sparse_attn_bwd / dsa_layer_bwd need when
  * they are called without o_acc: one fp32 value per (query, head),
@@ -158,6 +167,29 @@ dsa_status dsa_indexer_score(const dsa_dims *dims, const void *q_idx, const void
 dsa_status dsa_topk(const dsa_dims *dims, const float *scores, int64_t q_begin, int64_t q_count,
                     int32_t *idx, dsa_stream_t stream);
 
+/* Indexer scores and top-k selection of queries q_begin .. q_begin+q_count-1
+ * in one call: the same idx rows as dsa_indexer_score followed by dsa_topk,
+ * bit for bit.  Same page, "Model and bottleneck" (the quadratic scoring of
+ * every causal pool) and "1. DSA truly sparse" (scored per query chunk; only
+ * int32 pool indices leave the indexer).  Two routes for bf16 layers
+ * (dsa_set_indexer_topk_route); by default the score block is written to
+ * the workspace and selected from.  The other route does not materialise the
+ * fp32 score block: a tensor-core pass over every 32nd pool gives each row a
+ * threshold below its k-th score (with high probability), the full
+ * tensor-core pass keeps only the scores at or above it as candidates, and
+ * the exact selection (ties to the lower pool index) runs on those.  A row
+ * whose candidates number fewer than k, or overflow their fixed share of the
+ * candidate lists, is recomputed through the score block in the workspace and
+ * the row-wise top-k, so the result never depends on the threshold; only the
+ * time does.  fp32 layers run the unfused pair with the score block in ws.
+ *   idx  [L, k] int32; rows q_begin .. q_begin+q_count-1 are written
+ *   ws   >= dsa_indexer_topk_workspace_bytes(dims, q_count) bytes of device
+ *        memory (scratch; nothing in it needs to start at zero)
+ * Requires 0 <= q_begin, q_count >= 1, q_begin+q_count <= L. */
+dsa_status dsa_indexer_topk(const dsa_dims *dims, const void *q_idx, const void *kpool, const float *w,
+                            int64_t q_begin, int64_t q_count, int32_t *idx, void *ws, size_t ws_bytes,
+                            dsa_stream_t stream);
+
 /* Sparse attention forward over keys(t).  Same page, "1. DSA truly sparse"
  * (sparse kernel, NoPE, 2051 keys).  One K/V head shared by all Hq heads.
  *   q     [L, Hq, d]  layer dtype        k, v [L, d] layer dtype
@@ -191,7 +223,8 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims *dims, const void *q, const void *
                                dsa_stream_t stream);
 
 /* Whole forward: dsa_pool_keys once, then per chunk of q_chunk queries
- * dsa_indexer_score -> dsa_topk into the workspace, then dsa_sparse_attn_fwd.
+ * dsa_indexer_topk (the fused indexer + top-k) in the workspace, then
+ * dsa_sparse_attn_fwd.
  *   outputs: o [L,Hq,d], lse [L,Hq], idx [L,k], kpool [L/4,di];
  *            o_acc [L,Hq,d] fp32 when non-NULL (as in dsa_sparse_attn_fwd)
  *   ws      >= dsa_workspace_bytes(dims) bytes of device memory */
@@ -214,6 +247,16 @@ dsa_status dsa_layer_bwd(const dsa_dims *dims, const void *q, const void *k, con
  * bounded wait gave up; the kernel freed its resources and returned),
  * DSA_ERR_BAD_INDEX, or DSA_ERR_CUDA if the synchronisation itself failed. */
 dsa_status dsa_check_device_error(dsa_stream_t stream);
+
+/* Test and measurement hook: the route dsa_indexer_topk (and so
+ * dsa_layer_fwd) takes for bf16 layers.  Both give the same idx bit for bit.
+ *   1 (default): the indexer writes the chunk's fp32 score block into the
+ *      workspace and the row-wise top-k selects from it (dsa_indexer_score
+ *      then dsa_topk).
+ *   0: no score block; the candidate lists described at dsa_indexer_topk.
+ * Applies to calls made afterwards from any host thread.  Returns
+ * DSA_ERR_INVALID_ARG for any other value. */
+dsa_status dsa_set_indexer_topk_route(int32_t route);
 
 /* Test hook: the number of spin iterations after which a bounded device-side
  * wait gives up (default 1<<20).  Independently of this, every device wait

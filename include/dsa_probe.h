@@ -24,24 +24,27 @@
 extern "C" {
 #endif
 
-/* Replay the memory traffic of `steps` 16-key attention steps.
- *   d      head dim, 64 or 128
- *   L      rows of k, v (and of dk, dv); a multiple of 4, >= 4
+/* Replay the memory traffic of the sparse attention kernels for a given
+ * selection, with no arithmetic.
+ *   dims   the layer (bf16; d, Hq, k and L as for dsa_sparse_attn_fwd)
  *   k, v   [L, d] bf16 (read)
+ *   idx    [L, k] int32, the selection the attention kernels would use
  *   dk, dv [L, d] fp32, or both NULL.  When given, they are ADDED to (the
  *          probe adds tiny values; their contents are meaningless afterwards)
- *   steps  >= 1
- *   seed   selects the pseudo-random pools
- * One step picks 4 pools uniformly at random (a counter-based hash of seed,
- * step and slot) and gathers their 16 K rows and 16 V rows with the same
- * 16-byte cp.async copies the attention kernels use (16 * 2 * d * 2 bytes).
- * With dk/dv it then adds 4 * d fp32 values per pool into each of dk and dv
- * with one bulk (TMA-engine) reduction per pool and tensor, as the backward
- * does (16 * 2 * d * 4 bytes).  Returns DSA_OK, DSA_ERR_INVALID_ARG (NULL or
- * misaligned pointer, only one of dk/dv, bad L or steps), DSA_ERR_UNSUPPORTED
- * (d) or DSA_ERR_CUDA. */
-dsa_status dsa_probe_traffic(int32_t d, int64_t L, const void *k, const void *v, float *dk, float *dv,
-                             int64_t steps, uint64_t seed, dsa_stream_t stream);
+ * For every (query, 16-head group) one warp walks the same 16-key steps as
+ * the attention kernels (the pools of idx[t] in order, then the query's own
+ * partial pool), gathering each step's K and V rows with the same 16-byte
+ * cp.async copies, with the forward's warps per CTA, gather stages and CTAs
+ * per SM.  With dk/dv it also adds each pool slot's visible rows into dk and
+ * dv with one bulk (TMA-engine) fp32 reduction per slot and tensor, as the
+ * backward does, with the backward's occupancy.  The bytes moved are the
+ * kernels' logical bytes: 2*d*2 per attended key gathered, plus 2*d*4 per
+ * attended key reduced.  idx entries outside 0..elig(t)-1 are skipped.
+ * Returns DSA_OK, DSA_ERR_INVALID_ARG (NULL or misaligned pointer, only one
+ * of dk/dv), DSA_ERR_UNSUPPORTED (a shape the bf16 attention kernels do not
+ * take) or DSA_ERR_CUDA. */
+dsa_status dsa_probe_traffic(const dsa_dims *dims, const void *k, const void *v, const int32_t *idx, float *dk,
+                             float *dv, dsa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -7,8 +7,9 @@ memory and streams only).  There is no CPU path: if the library is missing
 or no GPU is present, calls raise.
 
 Entry points (same names as the C ABI, without the ``dsa_`` prefix):
-pool_keys, indexer_score, topk, sparse_attn_fwd, sparse_attn_bwd,
-layer_fwd, layer_bwd, check_device_error, workspace_bytes, bwd_workspace_bytes,
+pool_keys, indexer_score, topk, indexer_topk, sparse_attn_fwd, sparse_attn_bwd,
+layer_fwd, layer_bwd, check_device_error, workspace_bytes, indexer_topk_workspace_bytes,
+bwd_workspace_bytes,
 validate_dims, layer_fwd_noalloc; and the measurement probe probe_traffic
 (``include/dsa_probe.h``).
 """
@@ -68,6 +69,8 @@ def _load():
             "dsa_pool_keys": ([D, P, P, P], ctypes.c_int),
             "dsa_indexer_score": ([D, P, P, P, i64, i64, P, P], ctypes.c_int),
             "dsa_topk": ([D, P, i64, i64, P, P], ctypes.c_int),
+            "dsa_indexer_topk": ([D, P, P, P, i64, i64, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_indexer_topk_workspace_bytes": ([D, i64], ctypes.c_size_t),
             "dsa_sparse_attn_fwd": ([D, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_sparse_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -75,8 +78,9 @@ def _load():
             "dsa_layer_fwd_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
+            "dsa_set_indexer_topk_route": ([i32], ctypes.c_int),
             "dsa_selftest_bounded_wait": ([u32, P], ctypes.c_int),
-            "dsa_probe_traffic": ([i32, i64, P, P, P, P, i64, ctypes.c_uint64, P], ctypes.c_int),
+            "dsa_probe_traffic": ([D, P, P, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -157,6 +161,18 @@ def topk(dims, scores, q_begin, q_count, idx, stream=None):
                             _stream(stream)), "dsa_topk")
 
 
+def indexer_topk_workspace_bytes(dims, q_count) -> int:
+    return int(_load().dsa_indexer_topk_workspace_bytes(ctypes.byref(dims), int(q_count)))
+
+
+def indexer_topk(dims, q_idx, kpool, w, q_begin, q_count, idx, ws, ws_bytes=None, stream=None):
+    """Fused indexer + top-k of one query range (no score block for bf16 layers)."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(_load().dsa_indexer_topk(ctypes.byref(dims), _ptr(q_idx), _ptr(kpool), _ptr(w), int(q_begin), int(q_count),
+                                    _ptr(idx), _ptr(ws), int(ws_bytes), _stream(stream)), "dsa_indexer_topk")
+
+
 def sparse_attn_fwd(dims, q, k, v, idx, o, lse, stream=None, o_acc=None):
     """o_acc: optional fp32 [L, Hq, d] output (O with P carried beyond bf16)."""
     _check(_load().dsa_sparse_attn_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
@@ -199,10 +215,15 @@ def check_device_error(stream=None):
     _check(_load().dsa_check_device_error(_stream(stream)), "dsa_check_device_error")
 
 
-def probe_traffic(d, L, k, v, dk, dv, steps, seed=0, stream=None):
-    """Replay the attention kernels' L2 traffic with no arithmetic (include/dsa_probe.h)."""
-    _check(_load().dsa_probe_traffic(int(d), int(L), _ptr(k), _ptr(v), _ptr(dk), _ptr(dv), int(steps), int(seed),
+def probe_traffic(dims, k, v, idx, dk=None, dv=None, stream=None):
+    """Replay the attention kernels' memory traffic for a selection, with no arithmetic (include/dsa_probe.h)."""
+    _check(_load().dsa_probe_traffic(ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(idx), _ptr(dk), _ptr(dv),
                                      _stream(stream)), "dsa_probe_traffic")
+
+
+def set_indexer_topk_route(route: int):
+    """Route of the bf16 indexer + top-k: 1 score block + sampled thresholds (default), 0 candidate lists."""
+    _check(_load().dsa_set_indexer_topk_route(int(route)), "dsa_set_indexer_topk_route")
 
 
 def set_wait_limit(spins: int):

@@ -40,6 +40,7 @@ int device_sm_count() {
 namespace {
 
 thread_local char g_msg[512] = "";
+int g_indexer_topk_route = 1;   // see dsa_set_indexer_topk_route
 
 dsa_status fail(dsa_status st, const char* fmt, ...) {
   va_list ap;
@@ -114,6 +115,26 @@ dsa_status do_score(const dsa_dims* d, const void* q_idx, const void* kpool, con
 dsa_status do_topk(const dsa_dims* d, const float* scores, int64_t q_begin, int64_t q_count, int32_t* idx,
                    cudaStream_t s) {
   return cuda_status(dsa::launch_topk(d->L, d->k, scores, q_begin, q_count, idx, s), "topk launch");
+}
+
+size_t indexer_topk_ws_bytes(const dsa_dims* d, int64_t rows) {
+  if (is_bf16(d)) return dsa::fused_indexer_topk_ws_bytes(d->L, rows);
+  const size_t bytes = (size_t)rows * (size_t)(d->L / 4) * sizeof(float);   // the score block
+  return (bytes + 255) & ~(size_t)255;
+}
+
+// Indexer + top-k of one query range: fused (no score block) for bf16 layers,
+// the unfused pair through the score block in ws for fp32 layers.
+dsa_status do_indexer_topk(const dsa_dims* d, const void* q_idx, const void* kpool, const float* w, int64_t q_begin,
+                           int64_t q_count, int32_t* idx, void* ws, cudaStream_t s) {
+  if (!is_bf16(d)) {
+    dsa_status st = do_score(d, q_idx, kpool, w, q_begin, q_count, static_cast<float*>(ws), s);
+    if (st) return st;
+    return do_topk(d, static_cast<float*>(ws), q_begin, q_count, idx, s);
+  }
+  return cuda_status(dsa::launch_indexer_topk_bf16(d->L, d->Hi, d->di, d->k, q_idx, kpool, w, q_begin, q_count, idx,
+                                                   ws, g_indexer_topk_route, s),
+                     "indexer_topk launch");
 }
 
 dsa_status do_fwd(const dsa_dims* d, const void* q, const void* k, const void* v, const int32_t* idx, void* o,
@@ -203,10 +224,31 @@ dsa_status dsa_validate_dims(const dsa_dims* dims, int32_t with_backward) {
 
 size_t dsa_workspace_bytes(const dsa_dims* dims) {
   if (check_dims(dims, false) != DSA_OK) return 0;
-  const int64_t P = dims->L / 4;
   const int64_t C = dims->q_chunk < dims->L ? dims->q_chunk : dims->L;
-  const size_t bytes = (size_t)C * (size_t)P * sizeof(float);
-  return (bytes + 255) & ~(size_t)255;
+  return indexer_topk_ws_bytes(dims, C);
+}
+
+size_t dsa_indexer_topk_workspace_bytes(const dsa_dims* dims, int64_t q_count) {
+  if (check_dims(dims, false) != DSA_OK || q_count < 1 || q_count > dims->L) return 0;
+  return indexer_topk_ws_bytes(dims, q_count);
+}
+
+dsa_status dsa_indexer_topk(const dsa_dims* dims, const void* q_idx, const void* kpool, const float* w,
+                            int64_t q_begin, int64_t q_count, int32_t* idx, void* ws, size_t ws_bytes,
+                            dsa_stream_t stream) {
+  g_msg[0] = 0;
+  dsa_status st = check_dims(dims, false);
+  if (st) return st;
+  if ((st = check_range(dims, q_begin, q_count))) return st;
+  REQUIRE_PTR(q_idx);
+  REQUIRE_PTR(kpool);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(idx);
+  const size_t need = indexer_topk_ws_bytes(dims, q_count);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", ws_bytes, need);
+  if (!aligned16(ws)) return fail(DSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  return do_indexer_topk(dims, q_idx, kpool, w, q_begin, q_count, idx, ws, (cudaStream_t)stream);
 }
 
 dsa_status dsa_pool_keys(const dsa_dims* dims, const void* k_idx, void* kpool, dsa_stream_t stream) {
@@ -303,12 +345,10 @@ dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, con
   if (!aligned16(ws)) return fail(DSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   cudaStream_t s = (cudaStream_t)stream;
   if ((st = do_pool(dims, k_idx, kpool, s))) return st;
-  float* scores = static_cast<float*>(ws);
   const int64_t C = dims->q_chunk;
   for (int64_t q0 = 0; q0 < dims->L; q0 += C) {
     const int64_t n = dims->L - q0 < C ? dims->L - q0 : C;
-    if ((st = do_score(dims, q_idx, kpool, w, q0, n, scores, s))) return st;
-    if ((st = do_topk(dims, scores, q0, n, idx, s))) return st;
+    if ((st = do_indexer_topk(dims, q_idx, kpool, w, q0, n, idx, ws, s))) return st;
   }
   return do_fwd(dims, q, k, v, idx, o, lse, o_acc, s);
 }
@@ -337,6 +377,13 @@ dsa_status dsa_selftest_bounded_wait(uint32_t spins, dsa_stream_t stream) {
   if (spins == 0 || spins > (1u << 24)) return fail(DSA_ERR_INVALID_ARG, "spins must be in 1..2^24");
   dsa::selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(spins);
   return cuda_status(cudaGetLastError(), "selftest launch");
+}
+
+dsa_status dsa_set_indexer_topk_route(int32_t route) {
+  g_msg[0] = 0;
+  if (route != 0 && route != 1) return fail(DSA_ERR_INVALID_ARG, "route must be 0 or 1");
+  g_indexer_topk_route = route;
+  return DSA_OK;
 }
 
 void dsa_set_wait_limit(uint32_t spins) {

@@ -317,8 +317,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
       stage = stage == C::NST - 1 ? 0 : stage + 1;
       continue;
     }
-    // P and scale*dS as bf16 hi + lo (rows g: elements 0,1; rows g+8: 2,3);
-    // the dQ product takes the hi part of scale*dS only
+    // P and scale*dS as bf16 hi + lo (rows g: elements 0,1; rows g+8: 2,3)
     uint32_t pp[2][2], pl[2][2], dd[2][2], dl[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -334,7 +333,9 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
       split_bf16x2_bwd(s0, s1, dd[nt][0], dl[nt][0]);
       split_bf16x2_bwd(s2, s3, dd[nt][1], dl[nt][1]);
     }
-    // dQ += scale*dS K   (A = dS rows=heads, B = K^T via transposed loads)
+    // dQ += scale*dS K   (A = dS rows=heads, hi and lo parts; B = K^T via
+    // transposed loads).  A needle query's dQ sums large dS K terms, so the
+    // bf16 rounding of dS alone (2^-9) is not enough there.
     {
       const int mtx = lane >> 3, r = lane & 7;
       const int key = (mtx & 1) * 8 + r;
@@ -345,6 +346,8 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
         ldsm_x4_t(ks_base + key * C::ROW_BYTES + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
         mma_bf16_16816(dq[2 * j], dd[0][0], dd[0][1], dd[1][0], dd[1][1], b0, b1);
         mma_bf16_16816(dq[2 * j + 1], dd[0][0], dd[0][1], dd[1][0], dd[1][1], b2, b3);
+        mma_bf16_16816(dq[2 * j], dl[0][0], dl[0][1], dl[1][0], dl[1][1], b0, b1);
+        mma_bf16_16816(dq[2 * j + 1], dl[0][0], dl[0][1], dl[1][0], dl[1][1], b2, b3);
       }
     }
     // dV[keys] += P^T dO and dK[keys] += (scale*dS)^T Q   (rows = keys)

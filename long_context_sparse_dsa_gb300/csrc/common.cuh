@@ -26,6 +26,18 @@ __device__ __forceinline__ void record_error(unsigned bits) { atomicOr(&g_dev_er
 
 __device__ __forceinline__ int64_t elig(int64_t t) { return (t + 1) >> 2; }
 
+// Order-preserving uint32 key of an fp32 score (larger score -> larger key);
+// -0 is folded into +0 so the two tie.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The float whose order key is `key` (key must be the key of a finite value).
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -61,7 +61,8 @@ struct IdxCfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + NSA * A_BYTES;
   static constexpr int OFF_W = OFF_B + 2 * B_BYTES;
-  static constexpr int OFF_STG = OFF_W + NEPI * QPW * HI * 4;  // private w slice per epilogue warp
+  static constexpr int OFF_EMIT = OFF_W + NEPI * QPW * HI * 4;  // private w slice per epilogue warp
+  static constexpr int OFF_STG = OFF_EMIT + NEPI * QPW * 32;    // emit mode: per query {tau, cap, list base, length}
   static constexpr int NSTG = DI == 64 ? 2 : 1;            // score staging buffers per epilogue warp
   static constexpr int STG_BYTES = QPW * 32 * 4;           // QPW queries x 32 pools fp32
   static constexpr int OFF_BAR = OFF_STG + NEPI * NSTG * STG_BYTES;
@@ -94,24 +95,32 @@ __device__ __forceinline__ void tma_store_2d_commit_if(const void* tmap, uint32_
 }
 
 struct UnitIter {
-  int64_t q_begin, q_end, nqb, maxseg, P;
-  int64_t u, stride;
+  int64_t q_begin, q_end;
+  int nqb, maxseg;
+  int S;                      // column stride
+  const int32_t* blist;       // block-list mode when not null
+  int nlist;
+  int u, stride;
   // current unit
-  int64_t t0, tile_begin, tile_end;
-  __device__ int64_t ntiles(int64_t qb, int BN, int BM) const {
-    int64_t t_last = q_begin + qb * BN + BN - 1;
+  int64_t t0;
+  int tile_begin, tile_end;
+  // columns of the block row of query t: the pools p < elig(t) with p % S == 0
+  __device__ int64_t ncols(int64_t t) const { return S == 1 ? elig(t) : (elig(t) + S - 1) / S; }
+  __device__ int ntiles(int qb, int BN, int BM) const {
+    int64_t t_last = q_begin + (int64_t)qb * BN + BN - 1;
     if (t_last >= q_end) t_last = q_end - 1;
-    return (elig(t_last) + BM - 1) / BM;
+    return (int)((ncols(t_last) + BM - 1) / BM);
   }
   template <int BN, int BM, int SEG>
   __device__ bool next() {
-    while (u < nqb * maxseg) {
-      const int64_t seg = u / nqb;
-      const int64_t qb = nqb - 1 - (u % nqb);
+    const int nb = blist ? nlist : nqb;
+    while (u < nb * maxseg) {
+      const int seg = u / nb;
+      const int qb = blist ? blist[u % nb] : nqb - 1 - (u % nb);
       u += stride;
-      const int64_t nt = ntiles(qb, BN, BM);
+      const int nt = ntiles(qb, BN, BM);
       if (seg * SEG >= nt) continue;
-      t0 = q_begin + qb * BN;
+      t0 = q_begin + (int64_t)qb * BN;
       tile_begin = seg * SEG;
       tile_end = tile_begin + SEG < nt ? tile_begin + SEG : nt;
       return true;
@@ -120,12 +129,15 @@ struct UnitIter {
   }
 };
 
-template <int HI, int DI>
+template <int HI, int DI, bool EMIT>
 __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kp,
-                      const __grid_constant__ CUtensorMap tmap_s, const float* __restrict__ w,
-                      float* __restrict__ scores, int64_t P, int64_t q_begin, int64_t q_count, int tma_store) {
+                      const __grid_constant__ CUtensorMap tmap_s, const IdxArgs a) {
   using C = IdxCfg<HI, DI>;
+  const float* __restrict__ w = a.w;
+  float* __restrict__ scores = a.scores;
+  const int64_t P = a.P_cols, q_begin = a.q_begin, q_count = a.q_count;
+  const int tma_store = a.tma_store;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
@@ -178,14 +190,16 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
   UnitIter it;
   it.q_begin = q_begin;
   it.q_end = q_end;
-  it.nqb = (q_count + C::BN - 1) / C::BN;
-  it.P = P;
+  it.nqb = (int)((q_count + C::BN - 1) / C::BN);
+  it.S = a.col_stride;
+  it.blist = a.blist;
+  it.nlist = a.blist ? (int)*a.blist_n : 0;
   {
-    const int64_t nt_last = it.ntiles(it.nqb - 1, C::BN, C::BM);
+    const int nt_last = it.ntiles(it.nqb - 1, C::BN, C::BM);
     it.maxseg = (nt_last + C::SEG - 1) / C::SEG;
   }
-  it.u = blockIdx.x;
-  it.stride = gridDim.x;
+  it.u = (int)blockIdx.x;
+  it.stride = (int)gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         for (int c = 0; c < C::KC; ++c)
           tma_load_2d(sB + bb * C::B_BYTES + c * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, (int32_t)(it.t0 * HI));
         ++b_iter;
-        for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+        for (int tile = it.tile_begin; tile < it.tile_end; ++tile) {
           const int s = a_iter % C::NSA;
           if (!(ok = mbar_wait(empty_a(s), ((a_iter / C::NSA) & 1) ^ 1, abort_flag))) break;
           mbar_arrive_expect_tx(full_a(s), C::A_BYTES);
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
       while (ok && it.next<C::BN, C::BM, C::SEG>()) {
         const int bb = b_iter & 1;
         if (!(ok = mbar_wait(full_b(bb), (b_iter >> 1) & 1, abort_flag))) break;
-        for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+        for (int tile = it.tile_begin; tile < it.tile_end; ++tile) {
           const int s = a_iter % C::NSA;
           const int ab = acc_iter & 1;
           if (!(ok = mbar_wait(full_a(s), (a_iter / C::NSA) & 1, abort_flag))) break;
@@ -265,6 +279,13 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     uint32_t acc_iter = 0;
     bool ok = true;
     float* w_mine = w_s + ew * C::QPW * HI;  // this warp's QPW queries x HI weights
+    // emit mode, per query of this warp (8 words): [0] tau, [4] sub-list
+    // capacity, [5..6] sub-list base (64-bit), [7] sub-list length so far
+    // (words 4..7 are read as one 16-byte vector).  The lengths live in
+    // shared memory rather than registers: they persist across tiles, and
+    // registers are what the epilogue's scoring math is short of.
+    uint32_t* emit_mine = reinterpret_cast<uint32_t*>(smem + C::OFF_EMIT) + ew * C::QPW * 8;
+    const uint32_t emit_sa = smem_u32(emit_mine);
     const uint32_t w_mine_s = smem_u32(w_mine);
     uint32_t stg_iter = 0;
     constexpr int NLD = C::QPW * HI / 16;    // 16-column TMEM loads per tile
@@ -274,8 +295,32 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         const int64_t t = it.t0 + qg * C::QPW + i / HI;
         w_mine[i] = t < q_end ? __ldg(w + t * HI + (i % HI)) : 0.f;
       }
+      // emit mode: the threshold and this warp's sub-list of each of its
+      // queries for this unit (segment seg, lane quarter `quarter`); +inf and
+      // capacity 0 past the range
+      if constexpr (EMIT) {
+        if (lane < C::QPW) {
+          const int64_t t = it.t0 + qg * C::QPW + lane;
+          const int64_t seg = it.tile_begin / C::SEG;
+          float th = INFINITY;
+          uint32_t cap = 0u;
+          int64_t base = 0;
+          if (t < q_end) {
+            th = __ldg(a.tau + (t - q_begin));
+            const int64_t e = elig(t);
+            const int64_t nseg = e > kSegPools ? (e + kSegPools - 1) / kSegPools : 1;
+            cap = (uint32_t)(a.cand_stride / (4 * nseg));
+            base = (t - q_begin) * a.cand_stride + (seg * 4 + quarter) * (int64_t)cap;
+          }
+          emit_mine[8 * lane] = __float_as_uint(th);
+          emit_mine[8 * lane + 4] = cap;
+          emit_mine[8 * lane + 5] = (uint32_t)base;
+          emit_mine[8 * lane + 6] = (uint32_t)(base >> 32);
+          emit_mine[8 * lane + 7] = 0u;
+        }
+      }
       __syncwarp();
-      for (int64_t tile = it.tile_begin; tile < it.tile_end; ++tile) {
+      for (int tile = it.tile_begin; tile < it.tile_end; ++tile) {
         const int ab = acc_iter & 1;
         if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
         tc_fence_after();
@@ -291,6 +336,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(tempty(ab), lane == 0);
+        const int64_t p = (int64_t)tile * C::BM + lane_base + lane;
         float acc[C::QPW];
 #pragma unroll
         for (int j = 0; j < C::QPW; ++j) acc[j] = 0.f;
@@ -304,8 +350,40 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
             acc[c / HI] = fmaf(fmaxf(v[c / 16][c % 16], 0.f), wq[e], acc[c / HI]);
           }
         }
-        const int64_t p = tile * C::BM + lane_base + lane;
-        if (tma_store) {
+        if constexpr (EMIT) {
+          // candidates: every eligible score >= the row's threshold goes to
+          // this warp's sub-list of the row (no atomics: the warp alone fills
+          // it, with a warp-uniform running length); entries past the
+          // capacity are counted but not stored (the row then takes the
+          // score-block path)
+          const uint32_t below = (1u << lane) - 1u;
+          const int pe = (int)p;
+#pragma unroll
+          const int tq0 = (int)(it.t0 + qg * C::QPW);   // this warp's first query
+          for (int j = 0; j < C::QPW; ++j) {
+            uint32_t th;
+            asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(th) : "r"(emit_sa + 32 * j));
+            const bool take = pe < ((tq0 + j + 1) >> 2) && acc[j] >= __uint_as_float(th);
+            // the ballot also orders this lane-0 read-modify-write of the
+            // length after every lane's earlier reads of it
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            if (m != 0u) {   // warp-uniform
+              uint32_t cap, blo, bhi, len;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                           : "=r"(cap), "=r"(blo), "=r"(bhi), "=r"(len)
+                           : "r"(emit_sa + 32 * j + 16));
+              const uint32_t pos = len + (uint32_t)__popc(m & below);
+              if (take && pos < cap) {
+                const int64_t base = (int64_t)(((uint64_t)bhi << 32) | blo);
+                a.cand[base + pos] = make_uint2(__float_as_uint(acc[j]), (uint32_t)pe);
+              }
+              __syncwarp();
+              if (lane == 0)
+                asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(emit_sa + 32 * j + 28), "r"(len + (uint32_t)__popc(m)));
+            }
+          }
+          __syncwarp();
+        } else if (tma_store) {
           // stage this warp's QPW queries x 32 pools and store them with one
           // TMA box; entries past a query's causal prefix inside the box are
           // written too (the top-k never reads them)
@@ -326,10 +404,18 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
           for (int j = 0; j < C::QPW; ++j) {
             const int64_t t = it.t0 + qg * C::QPW + j;
             // streaming store: the score block is read once, by the top-k
-            if (t < q_end && p < elig(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
+            if (t < q_end && p < it.ncols(t)) __stcs(scores + (t - q_begin) * P + p, acc[j]);
           }
         }
         ++acc_iter;
+      }
+      if constexpr (EMIT) {
+        // the unit's sub-list lengths (lane j: query j)
+        __syncwarp();
+        const uint32_t mine = lane < C::QPW ? emit_mine[8 * lane + 7] : 0u;
+        const int64_t t = it.t0 + qg * C::QPW + lane;
+        if (ok && lane < C::QPW && t < q_end)
+          a.cntq[((t - q_begin) * a.nseg_max + it.tile_begin / C::SEG) * 4 + quarter] = mine;
       }
     }
     if (!ok) *abort_flag = 1;
@@ -361,10 +447,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int HI, int DI>
-static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, const float* w, int64_t q_begin,
-                             int64_t q_count, float* scores, cudaStream_t s) {
+static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, IdxArgs a, bool emit,
+                             cudaStream_t s) {
   using C = IdxCfg<HI, DI>;
   const int64_t P = L / 4;
+  const int S = a.col_stride;
+  const int64_t P_src = (P + S - 1) / S;   // kpool rows the launch reads (every S-th pool)
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tq, tk;
@@ -379,8 +467,9 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
       return cudaErrorInvalidValue;
   }
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)P};
-    const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
+    // row j of this view is pool j*S
+    const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)P_src};
+    const cuuint64_t strides[1] = {(cuuint64_t)DI * 2 * (cuuint64_t)S};
     const cuuint32_t box[2] = {64, (cuuint32_t)C::BM};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kpool), dims, strides, box, estr,
@@ -388,46 +477,55 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // Score tiles go out through TMA when the row pitch allows it (P*4 a
+  // Score tiles go out through TMA when the row pitch allows it (P_cols*4 a
   // multiple of 16 bytes); otherwise with plain stores.
-  CUtensorMap ts;
-  int tma_store = 0;
-  if ((P % 4) == 0) {
-    const cuuint64_t dims[2] = {(cuuint64_t)P, (cuuint64_t)q_count};
-    const cuuint64_t strides[1] = {(cuuint64_t)P * 4};
+  CUtensorMap ts = tk;  // unused unless a TMA store map is made below
+  a.tma_store = 0;
+  if (!emit && (a.P_cols % 4) == 0) {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.P_cols, (cuuint64_t)a.q_count};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.P_cols * 4};
     const cuuint32_t box[2] = {32, (cuuint32_t)C::QPW};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, scores, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+    if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.scores, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    tma_store = 1;
-  } else {
-    ts = tk;  // unused
+    a.tma_store = 1;
   }
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<HI, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  auto kern = emit ? indexer_tc_kernel<HI, DI, true> : indexer_tc_kernel<HI, DI, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int64_t nqb = (q_count + C::BN - 1) / C::BN;
-  int64_t t_last = q_begin + q_count - 1;
-  const int64_t nt_last = (((t_last + 1) >> 2) + C::BM - 1) / C::BM;
+  const int64_t nqb = (a.q_count + C::BN - 1) / C::BN;
+  const int64_t t_last = a.q_begin + a.q_count - 1;
+  const int64_t nt_last = ((((t_last + 1) >> 2) + S - 1) / S + C::BM - 1) / C::BM;
   const int64_t units = nqb * ((nt_last + C::SEG - 1) / C::SEG);
   if (units == 0) return cudaSuccess;
   int64_t grid = device_sm_count();
-  if (grid > units) grid = units;
-  indexer_tc_kernel<HI, DI><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, ts, w, scores, P, q_begin,
-                                                                               q_count, tma_store);
+  if (a.blist == nullptr && grid > units) grid = units;   // a block list's length is known on the device only
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, tk, ts, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_tc_bf16_ex(int64_t L, int Hi, int di, const void* q_idx, const void* kpool,
+                                      const IdxArgs& a, bool emit, cudaStream_t s) {
+  if (Hi == 8 && di == 64) return launch_tc<8, 64>(L, q_idx, kpool, a, emit, s);
+  if (Hi == 8 && di == 128) return launch_tc<8, 128>(L, q_idx, kpool, a, emit, s);
+  if (Hi == 4 && di == 64) return launch_tc<4, 64>(L, q_idx, kpool, a, emit, s);
+  if (Hi == 4 && di == 128) return launch_tc<4, 128>(L, q_idx, kpool, a, emit, s);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_indexer_tc_bf16(int64_t L, int Hi, int di, const void* q_idx, const void* kpool,
                                    const float* w, int64_t q_begin, int64_t q_count, float* scores,
                                    cudaStream_t s) {
-  if (Hi == 8 && di == 64) return launch_tc<8, 64>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
-  if (Hi == 8 && di == 128) return launch_tc<8, 128>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
-  if (Hi == 4 && di == 64) return launch_tc<4, 64>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
-  if (Hi == 4 && di == 128) return launch_tc<4, 128>(L, q_idx, kpool, w, q_begin, q_count, scores, s);
-  return cudaErrorNotSupported;
+  IdxArgs a{};
+  a.w = w;
+  a.scores = scores;
+  a.P_cols = L / 4;
+  a.q_begin = q_begin;
+  a.q_count = q_count;
+  a.col_stride = 1;
+  return launch_indexer_tc_bf16_ex(L, Hi, di, q_idx, kpool, a, false, s);
 }
 
 }  // namespace dsa

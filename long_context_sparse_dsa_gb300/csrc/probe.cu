@@ -1,12 +1,13 @@
 // probe.cu -- traffic replay of the attention kernels (dsa_probe_traffic).
 //
 // The attention kernels are bound by L2 traffic: the 16-byte pool gathers of
-// K and V (a 64 MiB table at L=131072 that stays in L2) and, in the backward,
-// the fp32 bulk reductions of dK and dV rows.  This kernel moves the same
-// traffic with the same instructions -- gather_step16 for the copies, one
-// cp.reduce.async.bulk per pool and tensor -- and no arithmetic, so its rate
-// is the ceiling the attention kernels are measured against.  Pools are drawn
-// uniformly at random by a counter-based hash (splitmix64's finaliser).
+// K and V (a table of L*d*2*2 bytes that stays in L2 at L = 131072) and, in
+// the backward, the fp32 bulk reductions of dK and dV rows.  This kernel walks
+// the same steps over the same selection with the same instructions
+// (step_pools and gather_step16 for the copies, one cp.reduce.async.bulk per
+// pool slot and tensor) and the same occupancy, and does no arithmetic, so
+// its time is the floor for the kernels' data movement and its rate the
+// ceiling they are measured against.
 #include "../../include/dsa_probe.h"
 #include "common.cuh"
 #include "gather.cuh"
@@ -23,13 +24,6 @@ using namespace dsa;
 constexpr int kProbeWarps = 4;
 constexpr int kProbeStages = 2;
 constexpr int kProbeRedInFlight = 4;   // bulk groups a lane may still be reading before it issues more
-
-__device__ __forceinline__ uint64_t mix64(uint64_t x) {
-  x += 0x9E3779B97F4A7C15ull;
-  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
-  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-  return x ^ (x >> 31);
-}
 
 __device__ __forceinline__ void probe_red_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes, bool pred) {
   asm volatile(
@@ -51,18 +45,23 @@ struct ProbeCfg {
   static constexpr int RED_POOL = 4 * D * 4;   // one pool's fp32 rows
   static constexpr int WARP_BYTES = kProbeStages * GatherCfg<D>::STAGE_BYTES + (RED ? 4 * RED_POOL : 0);
   static constexpr int SMEM = kProbeWarps * WARP_BYTES;
-  static constexpr int CTAS_PER_SM = RED ? 2 : 3;
 };
 
 template <int D, bool RED>
 __global__ void __launch_bounds__(32 * kProbeWarps) probe_traffic_kernel(const __nv_bfloat16* __restrict__ K,
                                                                         const __nv_bfloat16* __restrict__ V,
+                                                                        const int32_t* __restrict__ idx,
                                                                         float* __restrict__ dK,
-                                                                        float* __restrict__ dV, int64_t P,
-                                                                        int64_t steps, uint64_t seed) {
+                                                                        float* __restrict__ dV, int64_t L, int Hq,
+                                                                        int k) {
   using C = ProbeCfg<D, RED>;
   extern __shared__ __align__(128) unsigned char probe_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HG = Hq / 16;
+  const int64_t items = L * HG;
+  const int64_t item = items - 1 - ((int64_t)blockIdx.x * kProbeWarps + warp);   // late queries first
+  if (item < 0) return;
+  const int64_t t = item / HG;
   const uint32_t wbase = smem_u32(probe_smem) + warp * C::WARP_BYTES;
   const uint32_t rbase = wbase + kProbeStages * GatherCfg<D>::STAGE_BYTES;
   if (RED) {
@@ -71,26 +70,35 @@ __global__ void __launch_bounds__(32 * kProbeWarps) probe_traffic_kernel(const _
     fence_proxy_async_shared();
     __syncwarp();
   }
+  const int32_t* irow = idx + t * k;
+  const int nsteps = (k + 1 + 3) / 4;   // k selected slots + the partial-pool slot
   const GatherLane<D> gl = gather_lane<D>(lane);
-  const int64_t nw = (int64_t)gridDim.x * kProbeWarps;
+  bool bad = false;
+  uint32_t pc[4];
+  step_pools(irow, k, 0, t, pc, bad);
+  gather_step16<D>(wbase, K, V, pc, gl);
+  cp_async_commit();
   int stage = 0;
-  for (int64_t s = (int64_t)blockIdx.x * kProbeWarps + warp; s < steps; s += nw) {
-    const uint64_t h = mix64(seed ^ (uint64_t)(s * 4 + (lane & 3)));
-    const uint32_t mine = ((uint32_t)(h % (uint64_t)P) << 3) | 4u;   // a whole pool, 4 visible rows
-    uint32_t slots[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) slots[i] = __shfl_sync(0xffffffffu, mine, i);
-    gather_step16<D>(wbase + stage * GatherCfg<D>::STAGE_BYTES, K, V, slots, gl);
+  for (int step = 0; step < nsteps; ++step) {
+    uint32_t pf[4] = {0u, 0u, 0u, 0u};
+    if (step + 1 < nsteps) {
+      step_pools(irow, k, step + 1, t, pf, bad);
+      gather_step16<D>(wbase + (stage ^ 1) * GatherCfg<D>::STAGE_BYTES, K, V, pf, gl);
+    }
     cp_async_commit();
     cp_async_wait<kProbeStages - 1>();
     __syncwarp();
     if (RED) {
-      const bool on = lane < 4;
-      probe_wait_read(on);
+      const uint32_t mine = (lane & 3) == 0 ? pc[0] : (lane & 3) == 1 ? pc[1] : (lane & 3) == 2 ? pc[2] : pc[3];
+      const bool on = lane < 4 && slot_nrows(mine) > 0;
+      probe_wait_read(lane < 4);
       const int64_t row = 4 * (int64_t)slot_pool(mine);
-      probe_red_add_f32(dV + row * D, rbase + (lane & 3) * C::RED_POOL, C::RED_POOL, on);
-      probe_red_add_f32(dK + row * D, rbase + (lane & 3) * C::RED_POOL, C::RED_POOL, on);
+      const uint32_t bytes = (uint32_t)(slot_nrows(mine) * D * 4);
+      probe_red_add_f32(dV + row * D, rbase + (lane & 3) * C::RED_POOL, bytes, on);
+      probe_red_add_f32(dK + row * D, rbase + (lane & 3) * C::RED_POOL, bytes, on);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pc[i] = pf[i];
     stage ^= 1;
   }
   cp_async_wait<0>();
@@ -98,18 +106,17 @@ __global__ void __launch_bounds__(32 * kProbeWarps) probe_traffic_kernel(const _
 }
 
 template <int D, bool RED>
-cudaError_t launch_probe(int64_t L, const void* k, const void* v, float* dk, float* dv, int64_t steps,
-                         uint64_t seed, cudaStream_t s) {
+cudaError_t launch_probe(const dsa_dims* d, const void* k, const void* v, const int32_t* idx, float* dk, float* dv,
+                         cudaStream_t s) {
   using C = ProbeCfg<D, RED>;
   auto kern = probe_traffic_kernel<D, RED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  int64_t grid = (int64_t)device_sm_count() * C::CTAS_PER_SM;
-  const int64_t need = (steps + kProbeWarps - 1) / kProbeWarps;
-  if (grid > need) grid = need;
-  kern<<<(unsigned)grid, 32 * kProbeWarps, C::SMEM, s>>>(static_cast<const __nv_bfloat16*>(k),
-                                                          static_cast<const __nv_bfloat16*>(v), dk, dv, L / 4,
-                                                          steps, seed);
+  const int64_t items = d->L * (d->Hq / 16);
+  const int64_t blocks = (items + kProbeWarps - 1) / kProbeWarps;
+  kern<<<(unsigned)blocks, 32 * kProbeWarps, C::SMEM, s>>>(static_cast<const __nv_bfloat16*>(k),
+                                                            static_cast<const __nv_bfloat16*>(v), idx, dk, dv, d->L,
+                                                            d->Hq, d->k);
   return cudaGetLastError();
 }
 
@@ -122,15 +129,14 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 
 }  // namespace
 
-extern "C" dsa_status dsa_probe_traffic(int32_t d, int64_t L, const void* k, const void* v, float* dk, float* dv,
-                                        int64_t steps, uint64_t seed, dsa_stream_t stream) {
+extern "C" dsa_status dsa_probe_traffic(const dsa_dims* dims, const void* k, const void* v, const int32_t* idx,
+                                        float* dk, float* dv, dsa_stream_t stream) {
   dsa::set_last_error_message("");
-  if (d != 64 && d != 128) return probe_fail(DSA_ERR_UNSUPPORTED, "dsa_probe_traffic: d must be 64 or 128");
-  if (L < 4 || L % 4 != 0 || L > ((int64_t)1 << 31))
-    return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: L must be a multiple of 4 in [4, 2^31]");
-  if (steps < 1) return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: steps must be >= 1");
-  if (!aligned16(k) || !aligned16(v))
-    return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: k and v must be 16-byte aligned device pointers");
+  dsa_status st = dsa_validate_dims(dims, 0);
+  if (st != DSA_OK) return st;
+  if (dims->dtype != DSA_BF16) return probe_fail(DSA_ERR_UNSUPPORTED, "dsa_probe_traffic: bf16 layers only");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(idx))
+    return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: k, v and idx must be 16-byte aligned device pointers");
   if ((dk == nullptr) != (dv == nullptr))
     return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: give both dk and dv, or neither");
   const bool red = dk != nullptr;
@@ -138,12 +144,10 @@ extern "C" dsa_status dsa_probe_traffic(int32_t d, int64_t L, const void* k, con
     return probe_fail(DSA_ERR_INVALID_ARG, "dsa_probe_traffic: dk and dv must be 16-byte aligned");
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  if (d == 128)
-    e = red ? launch_probe<128, true>(L, k, v, dk, dv, steps, seed, s)
-            : launch_probe<128, false>(L, k, v, dk, dv, steps, seed, s);
+  if (dims->d == 128)
+    e = red ? launch_probe<128, true>(dims, k, v, idx, dk, dv, s) : launch_probe<128, false>(dims, k, v, idx, dk, dv, s);
   else
-    e = red ? launch_probe<64, true>(L, k, v, dk, dv, steps, seed, s)
-            : launch_probe<64, false>(L, k, v, dk, dv, steps, seed, s);
+    e = red ? launch_probe<64, true>(dims, k, v, idx, dk, dv, s) : launch_probe<64, false>(dims, k, v, idx, dk, dv, s);
   if (e != cudaSuccess) {
     dsa::set_last_error_message(cudaGetErrorString(e));
     return DSA_ERR_CUDA;

@@ -53,16 +53,6 @@ constexpr int kSamples = 1024;
 constexpr int kStreamUnroll = 4;                      // 128-score groups a warp loads per iteration
 constexpr int kTieUnroll = 8;                         // 32-score groups per iteration when collecting ties
 
-__device__ __forceinline__ uint32_t order_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if (u == 0x80000000u) u = 0u;  // -0 ties with +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-// The float whose order key is `key` (key must be the key of a finite value).
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
 // Exclusive block-wide scan of one int per thread.  Returns the exclusive
 // prefix; *total receives the block sum.  Contains __syncthreads().
 __device__ __forceinline__ int block_excl_scan(int v, int* warp_buf, int* total) {
@@ -257,12 +247,10 @@ __device__ __forceinline__ void select_from_candidates(const uint32_t* cand_key,
   }
 }
 
-// Four CTAs per SM (64 registers a thread).  Five fit in shared memory
-// (about 45 KB each), but the 48-register cap that five need spills, and four
-// measured faster on long rows (1M tokens: -20%) and no slower at 128k.
-__global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
-                                                            int64_t q_begin, int64_t q_count,
-                                                            int32_t* __restrict__ idx) {
+// The selection of one row (row r of the score block, query q_begin + r),
+// done by the whole CTA.
+__device__ __forceinline__ void topk_row(const float* __restrict__ scores, int64_t P, int k, int64_t q_begin,
+                                         int64_t r, int32_t* __restrict__ idx) {
   __shared__ __align__(16) int hist[2048];
   __shared__ int warp_buf[32];
   __shared__ int sel[4];
@@ -274,8 +262,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const float* __re
   __shared__ uint32_t samples[kSamples];
 
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  // Longer rows (later queries) first.
-  const int64_t r = q_count - 1 - (int64_t)blockIdx.x;
   const int64_t t = q_begin + r;
   const int64_t n64 = elig(t);
   int32_t* out = idx + t * (int64_t)k;
@@ -574,10 +560,45 @@ __global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const float* __re
   }
 }
 
+// Four CTAs per SM (64 registers a thread).  Five fit in shared memory
+// (about 45 KB each), but the 48-register cap that five need spills, and four
+// measured faster on long rows (1M tokens: -20%) and no slower at 128k.
+__global__ void __launch_bounds__(kTopkThreads, 4) topk_kernel(const float* __restrict__ scores, int64_t P, int k,
+                                                            int64_t q_begin, int64_t q_count,
+                                                            int32_t* __restrict__ idx) {
+  // Longer rows (later queries) first.
+  topk_row(scores, P, k, q_begin, q_count - 1 - (int64_t)blockIdx.x, idx);
+}
+
+// The same selection for the rows listed in rlist[0 .. *rlist_n) (the rows
+// the fused indexer + top-k could not settle from their candidates), by a
+// persistent grid; with an empty list every CTA returns at once.
+__global__ void __launch_bounds__(kTopkThreads, 4) topk_list_kernel(const float* __restrict__ scores, int64_t P,
+                                                                 int k, int64_t q_begin,
+                                                                 const int32_t* __restrict__ rlist,
+                                                                 const uint32_t* __restrict__ rlist_n,
+                                                                 int32_t* __restrict__ idx) {
+  const uint32_t n = *rlist_n;
+  for (uint32_t b = blockIdx.x; b < n; b += gridDim.x) {
+    topk_row(scores, P, k, q_begin, rlist[b], idx);
+    __syncthreads();   // the shared arrays are reused by the next row
+  }
+}
+
 cudaError_t launch_topk(int64_t L, int k, const float* scores, int64_t q_begin, int64_t q_count, int32_t* idx,
                         cudaStream_t s) {
   const int64_t P = L / 4;
   topk_kernel<<<(unsigned)q_count, kTopkThreads, 0, s>>>(scores, P, k, q_begin, q_count, idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_list(int64_t L, int k, const float* scores, int64_t q_begin, int64_t max_rows,
+                             const int32_t* rlist, const uint32_t* rlist_n, int32_t* idx, cudaStream_t s) {
+  const int64_t P = L / 4;
+  int64_t grid = (int64_t)device_sm_count() * 4;
+  if (grid > max_rows) grid = max_rows;
+  if (grid < 1) grid = 1;
+  topk_list_kernel<<<(unsigned)grid, kTopkThreads, 0, s>>>(scores, P, k, q_begin, rlist, rlist_n, idx);
   return cudaGetLastError();
 }
 

@@ -64,10 +64,25 @@ def test_bwd_workspace_bytes(lib):
     assert dsa.bwd_workspace_bytes(_dims(Hq=8, dtype="fp32")) == 0     # no fp32 backward
 
 
+def _fused_ws(C, P):
+    """The documented parts of the fused indexer + top-k workspace, each rounded up to 256 bytes."""
+    a = lambda b: (b + 255) // 256 * 256
+    nb = (C + 31) // 32
+    nseg = (P + 2047) // 2048
+    stride = max(4096, 64 * nseg)
+    return (a(C * P * 4) + a(C * ((P + 31) // 32) * 4) + a(C * stride * 8) + a(C * nseg * 16)
+            + 2 * a(C * 4) + 2 * a(nb * 4) + a(16))   # scores, samples, candidates, lengths, tau, row list, blocks
+
+
 def test_workspace_bytes(lib):
-    assert dsa.workspace_bytes(_dims(L=131072, q_chunk=8192)) == 8192 * 32768 * 4
-    assert dsa.workspace_bytes(_dims(L=4096, q_chunk=100)) == (100 * 1024 * 4 + 255) // 256 * 256
+    assert dsa.workspace_bytes(_dims(L=131072, q_chunk=8192)) == _fused_ws(8192, 32768)
+    assert dsa.workspace_bytes(_dims(L=4096, q_chunk=100)) == _fused_ws(100, 1024)
+    assert dsa.indexer_topk_workspace_bytes(_dims(L=4096, q_chunk=100), 37) == _fused_ws(37, 1024)
+    # fp32 layers run the unfused pair: the score block only
+    assert dsa.workspace_bytes(_dims(L=4096, q_chunk=100, Hq=8, dtype="fp32")) == (100 * 1024 * 4 + 255) // 256 * 256
     assert dsa.workspace_bytes(_dims(L=4094)) == 0
+    assert dsa.indexer_topk_workspace_bytes(_dims(L=4096), 0) == 0
+    assert dsa.indexer_topk_workspace_bytes(_dims(L=4096), 4097) == 0
 
 
 def test_null_and_misaligned_pointers_fail_before_launch(lib):
@@ -82,6 +97,14 @@ def test_null_and_misaligned_pointers_fail_before_launch(lib):
     # an empty query range is an error, not a silent no-op
     assert lib.dsa_topk(ctypes.byref(d), 256, 0, 0, 256, None) == dsa.DSA_ERR_INVALID_ARG
     assert lib.dsa_indexer_score(ctypes.byref(d), 256, 256, 256, 8, 0, 256, None) == dsa.DSA_ERR_INVALID_ARG
+    # the fused indexer + top-k: range, pointers and workspace are checked before any launch
+    p = ctypes.c_void_p(256)
+    assert lib.dsa_indexer_topk(ctypes.byref(d), p, p, p, 4000, 200, p, p, 1 << 40, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_topk(ctypes.byref(d), p, None, p, 0, 200, p, p, 1 << 40, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_topk(ctypes.byref(d), p, p, p, 0, 200, p, p, 16, None) == dsa.DSA_ERR_WORKSPACE
+    assert lib.dsa_indexer_topk(ctypes.byref(d), p, p, p, 0, 200, p, None, 1 << 40, None) == dsa.DSA_ERR_WORKSPACE
+    assert lib.dsa_indexer_topk(ctypes.byref(d), p, p, p, 0, 200, p, ctypes.c_void_p(264), 1 << 40, None) == \
+        dsa.DSA_ERR_INVALID_ARG
     # too small a workspace is reported as such
     p = ctypes.c_void_p(256)
     assert lib.dsa_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, None, p, p, p, 16, None) == \
@@ -126,13 +149,15 @@ def test_noalloc_checks_every_pointer_before_anything_is_enqueued(lib):
 def test_probe_validates_before_launch(lib):
     p, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)
     f = lib.dsa_probe_traffic
-    assert f(96, 4096, p, p, None, None, 10, 0, None) == dsa.DSA_ERR_UNSUPPORTED
-    assert f(128, 4094, p, p, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
-    assert f(128, 4096, p, p, None, None, 0, 0, None) == dsa.DSA_ERR_INVALID_ARG
-    assert f(128, 4096, None, p, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
-    assert f(128, 4096, p, odd, None, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
-    assert f(128, 4096, p, p, p, None, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG      # only one of dk/dv
-    assert f(128, 4096, p, p, p, odd, 10, 0, None) == dsa.DSA_ERR_INVALID_ARG
+    d = _dims()
+    assert f(ctypes.byref(_dims(d=96)), p, p, p, None, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(ctypes.byref(_dims(Hq=8, dtype="fp32")), p, p, p, None, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert f(ctypes.byref(_dims(L=4094)), p, p, p, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), None, p, p, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), p, odd, p, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), p, p, None, None, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), p, p, p, p, None, None) == dsa.DSA_ERR_INVALID_ARG      # only one of dk/dv
+    assert f(ctypes.byref(d), p, p, p, p, odd, None) == dsa.DSA_ERR_INVALID_ARG
 
 
 def test_binding_has_no_cpu_path():

@@ -60,24 +60,32 @@ def test_bounded_wait_gives_up_and_stream_survives():
 
 
 # ---------------------------------------------------------------- traffic probe
-@pytest.mark.parametrize("d", [64, 128])
-def test_probe_traffic_does_its_reductions(d):
+@pytest.mark.parametrize("Hq,d", [(16, 64), (32, 128)])
+def test_probe_traffic_does_its_reductions(Hq, d):
     """The traffic replay behind the attention kernels' roofline does the work
-    it claims: every step adds 4 pools x 4 rows x d values into each of dK and
-    dV, so their sums grow by exactly that count times the added value."""
-    L, steps = 4096, 5000
-    k = torch.randn(L, d, device=DEV).to(torch.bfloat16)
-    v = torch.randn(L, d, device=DEV).to(torch.bfloat16)
+    it claims: every (query, 16-head group) adds each of its attended keys'
+    rows (d values) once into dK and once into dV, so their sums grow by
+    exactly the attended-key count x head groups x d times the added value,
+    and only attended rows are touched."""
+    L, k = 3000, 32
+    Q, K, V, _, idx = _attn_case(L, Hq, d, k, "bf16", seed=41)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k)
+    kd, vd, idx_d = K.to(DEV), V.to(DEV), torch.from_numpy(idx).to(DEV)
     dk = torch.zeros(L, d, device=DEV)
     dv = torch.zeros(L, d, device=DEV)
-    dsa.probe_traffic(d, L, k, v, None, None, steps, seed=3)
-    dsa.probe_traffic(d, L, k, v, dk, dv, steps, seed=4)
+    dsa.probe_traffic(dims, kd, vd, idx_d)
+    dsa.probe_traffic(dims, kd, vd, idx_d, dk, dv)
     dsa.check_device_error()
-    want = steps * 16 * d * 1e-30
-    for t in (dk, dv):
-        got = float(t.double().sum())
+    hits = np.zeros(L, np.int64)
+    for t in range(L):
+        keys = oracle.key_set(t, idx[t], k)
+        np.add.at(hits, keys, 1)
+    want = float(hits.sum()) * (Hq // 16) * d * 1e-30
+    for tns in (dk, dv):
+        got = float(tns.double().sum())
         assert abs(got - want) <= 1e-3 * want, (got, want)
-        assert int((t != 0).any(1).sum()) > L // 2     # the pools are spread over the table
+        touched = (tns != 0).any(1).cpu().numpy()
+        assert np.array_equal(touched, hits > 0)
 
 
 # ---------------------------------------------------------------- pool keys
@@ -188,6 +196,93 @@ def test_topk_bitexact(kind, k):
         assert np.array_equal(got, ref), (q_begin, np.argwhere(got != ref)[:5])
         untouched = np.setdiff1d(np.arange(L), rows)[:50]
         assert np.all(idx.cpu().numpy()[untouched] == -7)
+
+
+# ---------------------------------------------------------------- fused indexer + top-k
+def _fused_vs_unfused(L, Hi, di, k, q_I, k_I, w, q_begin, q_count):
+    """idx rows from dsa_indexer_topk and from dsa_indexer_score + dsa_topk."""
+    dims = dsa.make_dims(L, 16, 128, Hi, di, k, q_chunk=q_count)
+    kp = torch.empty((L // 4, di), dtype=torch.bfloat16, device=DEV)
+    qd, wd = q_I.to(DEV), w.to(DEV)
+    dsa.pool_keys(dims, k_I.to(DEV), kp)
+    sc = torch.empty((q_count, L // 4), device=DEV)
+    ref = torch.full((L, k), -7, dtype=torch.int32, device=DEV)
+    dsa.indexer_score(dims, qd, kp, wd, q_begin, q_count, sc)
+    dsa.topk(dims, sc, q_begin, q_count, ref)
+    ws = torch.empty(dsa.indexer_topk_workspace_bytes(dims, q_count), dtype=torch.uint8, device=DEV)
+    ws.fill_(0xA5)                                  # nothing in the workspace may need to start at zero
+    outs = []
+    try:
+        for route in (0, 1):                        # candidate lists; score block + sampled thresholds
+            dsa.set_indexer_topk_route(route)
+            for _ in range(2):                      # the second call runs on a used workspace
+                got = torch.full((L, k), -7, dtype=torch.int32, device=DEV)
+                dsa.indexer_topk(dims, qd, kp, wd, q_begin, q_count, got, ws)
+                outs.append(got)
+    finally:
+        dsa.set_indexer_topk_route(1)
+    dsa.check_device_error()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    return outs[0].cpu().numpy(), ref.cpu().numpy(), kp
+
+
+@pytest.mark.parametrize("inputs", ["normal", "int"])
+@pytest.mark.parametrize("Hi,di,k", [(8, 64, 512), (4, 128, 64), (8, 128, 1024), (4, 64, 1)])
+def test_indexer_topk_equals_unfused(inputs, Hi, di, k):
+    """The fused indexer + top-k gives the unfused pair's idx bit for bit:
+    rows of every kind (elig <= k, kept whole, thresholded), a range that
+    starts and ends off the 32-query block, rows outside it untouched; with
+    integer inputs also the oracle's selection."""
+    g = torch.Generator().manual_seed(7 + Hi + di + k)
+    L = 4 * 9000 + 4 * 77
+    if inputs == "int":
+        q_I, k_I, w = _int_inputs(g, L, Hi, di, "bf16")
+    else:
+        q_I = torch.randn(L, Hi, di, generator=g).to(torch.bfloat16)
+        k_I = torch.randn(L, di, generator=g).to(torch.bfloat16)
+        w = torch.rand(L, Hi, generator=g)
+    for q_begin, q_count in ((0, 3000), (L - 5037, 5037)):
+        got, ref, kp = _fused_vs_unfused(L, Hi, di, k, q_I, k_I, w, q_begin, q_count)
+        assert np.array_equal(got, ref), (q_begin, np.argwhere(got != ref)[:5])
+        rows = np.arange(q_begin, q_begin + q_count)
+        outside = np.setdiff1d(np.arange(L), rows)
+        assert np.all(got[outside] == -7)
+        if inputs == "int":
+            sample = rows[:: max(1, q_count // 200)]
+            orc = oracle.topk(oracle.indexer_scores(_f32(q_I), _f32(kp), _f32(w), sample), L, k, sample)
+            assert np.array_equal(got[sample], orc)
+
+
+@pytest.mark.parametrize("case", ["all_tied", "threshold_misses"])
+def test_indexer_topk_fallback_rows(case):
+    """Rows the candidate lists cannot settle go through the score rows and
+    the row-wise top-k, with the same result.  all_tied: every score is 0, so
+    every eligible pool is a candidate and long rows overflow their lists
+    (the answer is pools 0..k-1).  threshold_misses: the sampled pools (every
+    32nd) score far above the rest, so the sampled threshold lets fewer than
+    k candidates through."""
+    L, Hi, di, k = 4 * 12000, 8, 64, 512
+    g = torch.Generator().manual_seed(99)
+    if case == "all_tied":
+        q_I = torch.zeros(L, Hi, di).to(torch.bfloat16)
+        k_I = torch.randint(-3, 4, (L, di), generator=g).to(torch.bfloat16)
+        w = torch.ones(L, Hi)
+    else:
+        q_I = torch.randint(1, 3, (L, Hi, di), generator=g).to(torch.bfloat16)
+        k_I = torch.randint(0, 2, (L, di), generator=g).to(torch.float32)
+        pool_of = torch.arange(L) // 4
+        k_I[(pool_of % 32) == 0] += 3.0
+        k_I = k_I.to(torch.bfloat16)
+        w = torch.randint(1, 5, (L, Hi), generator=g).to(torch.float32)
+    q_begin, q_count = L - 4096, 4096
+    got, ref, kp = _fused_vs_unfused(L, Hi, di, k, q_I, k_I, w, q_begin, q_count)
+    assert np.array_equal(got, ref)
+    rows = np.arange(q_begin, q_begin + q_count)[::97]
+    orc = oracle.topk(oracle.indexer_scores(_f32(q_I), _f32(kp), _f32(w), rows), L, k, rows)
+    assert np.array_equal(got[rows], orc)
+    if case == "all_tied":
+        assert np.array_equal(got[rows], np.tile(np.arange(k, dtype=np.int32), (rows.size, 1)))
 
 
 # ---------------------------------------------------------------- attention
