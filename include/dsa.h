@@ -222,6 +222,32 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims *dims, const void *q, const void *
                                const void *dout, float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
                                dsa_stream_t stream);
 
+/* Bytes of device workspace dsa_sparse_attn_bwd_det needs: D (L*Hq*4), the
+ * inverted selection (per-(pool, 1024-query block) offsets and the L*k query
+ * lists, int32) and one band's partial dK/dV sums.  Returns 0 if dims are
+ * invalid for a backward or L*(k+1) >= 2^31. */
+size_t dsa_bwd_det_workspace_bytes(const dsa_dims *dims);
+
+/* Deterministic sparse attention backward (bf16): the gradients of
+ * dsa_sparse_attn_bwd, with dK and dV summed in a fixed order, so repeated
+ * calls on the same inputs give the same bits.  Same page, section "Real
+ * data" (the trainer's log-probs are checked against the inference
+ * engine's, which wants gradients that do not change run to run).
+ * dQ is formed query-major as in dsa_sparse_attn_bwd.  For dK/dV the
+ * selection is inverted into per-pool query lists in ascending query order
+ * (no atomics decide the order), and per band of 4096 queries each pool's
+ * contributions are accumulated key-major in registers and added to dK/dV
+ * in a fixed (band, chunk, query) order.  Arguments as dsa_sparse_attn_bwd,
+ * except the workspace, which is always required:
+ *   ws   >= dsa_bwd_det_workspace_bytes(dims) bytes of device memory
+ *        (scratch; nothing in it needs to start at zero)
+ * idx entries outside 0..elig(t)-1 are skipped.  Returns
+ * DSA_ERR_UNSUPPORTED when L*(k+1) >= 2^31. */
+dsa_status dsa_sparse_attn_bwd_det(const dsa_dims *dims, const void *q, const void *k, const void *v,
+                                   const int32_t *idx, const void *o, const float *lse, const float *o_acc,
+                                   const void *dout, float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                                   dsa_stream_t stream);
+
 /* Whole forward: dsa_pool_keys once, then per chunk of q_chunk queries
  * dsa_indexer_topk (the fused indexer + top-k) in the workspace, then
  * dsa_sparse_attn_fwd.

@@ -7,7 +7,7 @@ memory and streams only).  There is no CPU path: if the library is missing
 or no GPU is present, calls raise.
 
 Entry points (same names as the C ABI, without the ``dsa_`` prefix):
-pool_keys, indexer_score, topk, indexer_topk, sparse_attn_fwd, sparse_attn_bwd,
+pool_keys, indexer_score, topk, indexer_topk, sparse_attn_fwd, sparse_attn_bwd, sparse_attn_bwd_det,
 layer_fwd, layer_bwd, check_device_error, workspace_bytes, indexer_topk_workspace_bytes,
 bwd_workspace_bytes,
 validate_dims, layer_fwd_noalloc; and the measurement probe probe_traffic
@@ -75,6 +75,8 @@ def _load():
             "dsa_sparse_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_fwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dsa_layer_bwd": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_sparse_attn_bwd_det": ([D, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dsa_bwd_det_workspace_bytes": ([D], ctypes.c_size_t),
             "dsa_layer_fwd_noalloc": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
@@ -186,6 +188,28 @@ def sparse_attn_bwd(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws=None, ws_by
     _check(_load().dsa_sparse_attn_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse),
                                        _ptr(o_acc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), int(ws_bytes),
                                        _stream(stream)), "dsa_sparse_attn_bwd")
+
+
+def bwd_det_workspace_bytes(dims) -> int:
+    return int(_load().dsa_bwd_det_workspace_bytes(ctypes.byref(dims)))
+
+
+def alloc_bwd_det_workspace(dims, device="cuda"):
+    import torch
+    n = bwd_det_workspace_bytes(dims)
+    if n == 0:
+        _check(validate_dims(dims, True), "dsa_bwd_det_workspace_bytes")
+        raise DSAError(DSA_ERR_UNSUPPORTED, "dsa_bwd_det_workspace_bytes", "L * (k + 1) >= 2^31")
+    return torch.empty((n,), dtype=torch.uint8, device=device)
+
+
+def sparse_attn_bwd_det(dims, q, k, v, idx, o, lse, dout, dq, dk, dv, ws, ws_bytes=None, stream=None, o_acc=None):
+    """Deterministic backward: dK/dV summed in a fixed order (bitwise reproducible)."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(_load().dsa_sparse_attn_bwd_det(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o),
+                                           _ptr(lse), _ptr(o_acc), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                           int(ws_bytes), _stream(stream)), "dsa_sparse_attn_bwd_det")
 
 
 def layer_fwd(dims, q, k, v, q_idx, k_idx, w, o, lse, idx, kpool, ws, ws_bytes=None, stream=None, o_acc=None):

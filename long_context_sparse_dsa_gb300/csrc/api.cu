@@ -333,6 +333,42 @@ dsa_status dsa_sparse_attn_bwd(const dsa_dims* dims, const void* q, const void* 
   return do_bwd(dims, q, k, v, idx, lse, nullptr, dout, dq, dk, dv, static_cast<float*>(ws), (cudaStream_t)stream);
 }
 
+size_t dsa_bwd_det_workspace_bytes(const dsa_dims* dims) {
+  if (check_dims(dims, true) != DSA_OK) return 0;
+  if ((int64_t)dims->L * (dims->k + 1) >= ((int64_t)1 << 31)) return 0;
+  return dsa::det_bwd_ws_bytes(dims->L, dims->Hq, dims->d, dims->k);
+}
+
+dsa_status dsa_sparse_attn_bwd_det(const dsa_dims* dims, const void* q, const void* k, const void* v,
+                                   const int32_t* idx, const void* o, const float* lse, const float* o_acc,
+                                   const void* dout, float* dq, float* dk, float* dv, void* ws, size_t ws_bytes,
+                                   dsa_stream_t stream) {
+  g_msg[0] = 0;
+  dsa_status st = check_dims(dims, true);
+  if (st) return st;
+  if ((int64_t)dims->L * (dims->k + 1) >= ((int64_t)1 << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "the deterministic backward needs L * (k + 1) < 2^31");
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(k);
+  REQUIRE_PTR(v);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(o);
+  REQUIRE_PTR(lse);
+  REQUIRE_PTR(dout);
+  REQUIRE_PTR(dq);
+  REQUIRE_PTR(dk);
+  REQUIRE_PTR(dv);
+  if (dk == dv) return fail(DSA_ERR_INVALID_ARG, "dk and dv must not alias");
+  if (o_acc != nullptr && !aligned16(o_acc)) return fail(DSA_ERR_INVALID_ARG, "o_acc is not 16-byte aligned");
+  const size_t need = dsa::det_bwd_ws_bytes(dims->L, dims->Hq, dims->d, dims->k);
+  if (ws == nullptr || ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", ws_bytes, need);
+  if (!aligned16(ws)) return fail(DSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  return cuda_status(dsa::launch_attn_bwd_det_bf16(dims->L, dims->Hq, dims->d, dims->k, dims->scale, q, k, v, idx,
+                                                    lse, dout, o_acc, dq, dk, dv, ws, (cudaStream_t)stream),
+                     "sparse_attn_bwd_det launch");
+}
+
 dsa_status dsa_layer_fwd(const dsa_dims* dims, const void* q, const void* k, const void* v, const void* q_idx,
                          const void* k_idx, const float* w, void* o, float* lse, float* o_acc, int32_t* idx,
                          void* kpool, void* ws, size_t ws_bytes, dsa_stream_t stream) {

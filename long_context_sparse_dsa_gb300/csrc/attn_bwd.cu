@@ -43,6 +43,9 @@ namespace dsa {
 
 // PASS 1 forms D[t,h] = sum_j P_j dP_j into a [L, Hq] fp32 buffer; PASS 2
 // forms dS and the gradients.  PASS 2 also keeps swizzled copies of Q and dO.
+// PASS 3 (the deterministic backward's query-major half) forms dQ only, and
+// when it takes D from o_acc it also stores D in the [L, Hq] buffer for the
+// key-major half.
 // Gather stages per warp and warps per CTA (two CTAs per SM either way:
 // shared memory allows 2 x 4 warps x 2 stages or 2 x 3 warps x 3 stages).
 // Measured at L=131072: 45.8 ms for two stages at four warps, 46.6 ms for
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
     cp_async_commit();
   }
   float Dg = 0.f, Dg8 = 0.f;
-  if (PASS == 2) {
+  if (PASS >= 2) {
     if (Oacc != nullptr) {
       // D = dO . O over this lane's dO fragment columns (ks*16 + 2qi + {0,1}
       // and ks*16 + 8 + 2qi + {0,1}), then summed over the quad
@@ -350,6 +353,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
         mma_bf16_16816(dq[2 * j + 1], dl[0][0], dl[0][1], dl[1][0], dl[1][1], b2, b3);
       }
     }
+    if constexpr (PASS == 2) {
     // dV[keys] += P^T dO and dK[keys] += (scale*dS)^T Q   (rows = keys)
     // transposed A operands (rows = keys): [0] the hi parts, [1] the lo parts
     uint32_t pt[2][4], dt[2][4];
@@ -435,6 +439,7 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
         bulk_red_add_f32_if(gdst + rrow_g * D, rsrc, rbytes, rok);
       }
     }
+    }
     __syncwarp();
     rotate_slots<C::NST>(pc, pn, pf);
     stage = stage == C::NST - 1 ? 0 : stage + 1;
@@ -444,6 +449,10 @@ __global__ void __launch_bounds__(32 * kBwdWarps) attn_bwd_bf16_kernel(
     bulk_wait<0>();   // every bulk reduction of this thread has completed before the CTA exits
   }
   if (bad_idx && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
+  if (PASS == 3 && Oacc != nullptr && qi == 0) {
+    Dbuf[row0 + g] = Dg;
+    Dbuf[row0 + g + 8] = Dg8;
+  }
   if (PASS == 1) {
     Dg += __shfl_xor_sync(0xffffffffu, Dg, 1);
     Dg += __shfl_xor_sync(0xffffffffu, Dg, 2);
@@ -480,6 +489,27 @@ static cudaError_t launch_pass(int64_t L, int Hq, int k, float scale, const __nv
   attn_bwd_bf16_kernel<D, PASS><<<(unsigned)blocks, 32 * C::WARPS, C::SMEM, s>>>(
       q, kk, v, idx, lse, dout, oacc, dbuf, dq, dk, dv, L, Hq, k, scale, scale_log2);
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_dq_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                    const void* v, const int32_t* idx, const float* lse, const void* dout,
+                                    const float* oacc, float* dbuf, float* dq, cudaStream_t s) {
+  auto qp = static_cast<const __nv_bfloat16*>(q);
+  auto kp = static_cast<const __nv_bfloat16*>(kk);
+  auto vp = static_cast<const __nv_bfloat16*>(v);
+  auto gp = static_cast<const __nv_bfloat16*>(dout);
+  cudaError_t e = cudaSuccess;
+  if (d == 128) {
+    if (oacc == nullptr) e = launch_pass<128, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, nullptr, dbuf, dq, nullptr, nullptr, s);
+    if (e == cudaSuccess) e = launch_pass<128, 3>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, oacc, dbuf, dq, nullptr, nullptr, s);
+    return e;
+  }
+  if (d == 64) {
+    if (oacc == nullptr) e = launch_pass<64, 1>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, nullptr, dbuf, dq, nullptr, nullptr, s);
+    if (e == cudaSuccess) e = launch_pass<64, 3>(L, Hq, k, scale, qp, kp, vp, idx, lse, gp, oacc, dbuf, dq, nullptr, nullptr, s);
+    return e;
+  }
+  return cudaErrorNotSupported;
 }
 
 template <int D>

@@ -93,6 +93,19 @@ cudaError_t launch_attn_bwd_bf16(int64_t L, int Hq, int d, int k, float scale, c
                                  const void* v, const int32_t* idx, const float* lse, const void* dout,
                                  const float* oacc, float* dbuf, float* dq, float* dk, float* dv, cudaStream_t s);
 
+// The query-major half of the deterministic backward: dQ, and D into dbuf
+// (formed from oacc when given, else by a first D pass).
+cudaError_t launch_attn_bwd_dq_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                    const void* v, const int32_t* idx, const float* lse, const void* dout,
+                                    const float* oacc, float* dbuf, float* dq, cudaStream_t s);
+
+// The deterministic (key-major) backward: dq, dk, dv overwritten; ws holds
+// det_bwd_ws_bytes(L, Hq, d, k) bytes of scratch.
+size_t det_bwd_ws_bytes(int64_t L, int Hq, int d, int k);
+cudaError_t launch_attn_bwd_det_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                     const void* v, const int32_t* idx, const float* lse, const void* dout,
+                                     const float* oacc, float* dq, float* dk, float* dv, void* ws, cudaStream_t s);
+
 int device_sm_count();
 
 }  // namespace dsa

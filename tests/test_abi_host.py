@@ -146,6 +146,24 @@ def test_noalloc_checks_every_pointer_before_anything_is_enqueued(lib):
             assert name.encode() in lib.dsa_last_error_message()
 
 
+def test_deterministic_backward_validates_before_launch(lib):
+    d = _dims()
+    p, q, odd = ctypes.c_void_p(256), ctypes.c_void_p(512), ctypes.c_void_p(264)
+    f = lib.dsa_sparse_attn_bwd_det
+    need = dsa.bwd_det_workspace_bytes(d)
+    assert need > 4096 * 512 * 4          # at least the inverted selection's query lists
+    #        q  k  v  idx o  lse o_acc dout dq dk dv ws ws_bytes
+    assert f(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, q, None, 0, None) == dsa.DSA_ERR_WORKSPACE
+    assert f(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, q, p, need - 1, None) == dsa.DSA_ERR_WORKSPACE
+    assert f(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, q, odd, need, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), p, p, p, None, p, p, None, p, p, p, q, p, need, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(d), p, p, p, p, p, p, None, p, p, p, p, p, need, None) == dsa.DSA_ERR_INVALID_ARG  # dk == dv
+    assert f(ctypes.byref(d), p, p, p, p, p, p, odd, p, p, p, q, p, need, None) == dsa.DSA_ERR_INVALID_ARG
+    assert f(ctypes.byref(_dims(Hq=8, dtype="fp32")), p, p, p, p, p, p, None, p, p, p, q, p, need, None) == \
+        dsa.DSA_ERR_UNSUPPORTED
+    assert dsa.bwd_det_workspace_bytes(_dims(L=1 << 22, k=1024)) == 0     # L * (k + 1) >= 2^31
+
+
 def test_probe_validates_before_launch(lib):
     p, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)
     f = lib.dsa_probe_traffic

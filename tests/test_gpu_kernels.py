@@ -326,6 +326,55 @@ def test_attn_fwd_matches_oracle(dtype, Hq, d, k):
         assert torch.equal(O2, O) and torch.equal(o_acc, O)
 
 
+def _bwd(det, dims, dev, idx_d, O, lse, dq, dk, dv, o_acc):
+    """The atomic backward (det=False) or the deterministic one (det=True)."""
+    if det:
+        ws = dsa.alloc_bwd_det_workspace(dims, DEV)
+        ws.fill_(0x5A)                              # nothing in it may need to start at zero
+        dsa.sparse_attn_bwd_det(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws, o_acc=o_acc)
+    else:
+        ws = None if o_acc is not None else dsa.alloc_backward_workspace(dims, DEV)
+        dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws, o_acc=o_acc)
+
+
+@pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64), (32, 64)])
+@pytest.mark.parametrize("k", [3, 32])
+@pytest.mark.parametrize("use_o_acc", [False, True])
+def test_attn_bwd_det_matches_oracle_and_repeats(Hq, d, k, use_o_acc):
+    """The deterministic backward: dQ, dK, dV within 2e-2 of the oracle, the
+    same bits on a second call (on a dirty workspace), and dQ bit-identical to
+    the atomic backward's (the same query-major arithmetic)."""
+    L = 1000
+    Q, K, V, dO, idx = _attn_case(L, Hq, d, k, "bf16", seed=60 + k)
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale)
+    dev = [t.to(DEV) for t in (Q, K, V, dO)]
+    idx_d = torch.from_numpy(idx).to(DEV)
+    O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    o_acc = torch.empty((L, Hq, d), device=DEV) if use_o_acc else None
+    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, o_acc=o_acc)
+    runs = []
+    for _ in range(2):
+        dq = torch.full((L, Hq, d), 3.0, device=DEV)
+        dk = torch.full((L, d), 5.0, device=DEV)    # overwritten, not accumulated into
+        dv = torch.full((L, d), 5.0, device=DEV)
+        _bwd(True, dims, dev, idx_d, O, lse, dq, dk, dv, o_acc)
+        runs.append((dq, dk, dv))
+    dsa.check_device_error()
+    for a, b in zip(runs[0], runs[1]):
+        assert torch.equal(a, b)
+    dq_a = torch.empty((L, Hq, d), device=DEV)
+    dk_a, dv_a = torch.empty((L, d), device=DEV), torch.empty((L, d), device=DEV)
+    _bwd(False, dims, dev, idx_d, O, lse, dq_a, dk_a, dv_a, o_acc)
+    dsa.check_device_error()
+    assert torch.equal(runs[0][0], dq_a)
+    dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
+    errs = {name: float(np.abs(got.cpu().numpy() - ref).max())
+            for name, got, ref in (("dQ", runs[0][0], dQr), ("dK", runs[0][1], dKr), ("dV", runs[0][2], dVr))}
+    assert max(errs.values()) <= 2e-2, errs
+
+
 @pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64)])
 @pytest.mark.parametrize("k", [3, 32])
 @pytest.mark.parametrize("use_o_acc", [False, True])
@@ -354,7 +403,8 @@ def test_attn_bwd_matches_oracle(Hq, d, k, use_o_acc):
 
 @pytest.mark.parametrize("case", ["dO_times_1e-6", "beyond_fp16_range", "unit_scale"])
 @pytest.mark.parametrize("use_o_acc", [False, True])
-def test_attn_bwd_scaled_inputs(case, use_o_acc):
+@pytest.mark.parametrize("det", [False, True])
+def test_attn_bwd_scaled_inputs(case, use_o_acc, det):
     """Inputs far from unit scale, compared element by element with the oracle.
 
     A loss-scaled upstream gradient (dO ~ 1e-6 per element) and Q / dO entries
@@ -385,8 +435,7 @@ def test_attn_bwd_scaled_inputs(case, use_o_acc):
     dq = torch.empty((L, Hq, d), device=DEV)
     dk = torch.empty((L, d), device=DEV)
     dv = torch.empty((L, d), device=DEV)
-    ws = None if use_o_acc else dsa.alloc_backward_workspace(dims, DEV)
-    dsa.sparse_attn_bwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, dev[3], dq, dk, dv, ws, o_acc=o_acc)
+    _bwd(det, dims, dev, idx_d, O, lse, dq, dk, dv, o_acc)
     dsa.check_device_error()
     dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
     grad_scale = {"dQ": sdO * sK, "dK": sdO * sQ, "dV": sdO}

@@ -233,19 +233,39 @@ def test_full_size_gradients_elementwise(name, record_property):
     gq = out["dq"].cpu().numpy()
     eq = float(np.abs(gq - dQ).max())
     del gq, dQ
+    # the deterministic backward on the same forward: the same bits twice, and
+    # the same oracle bound
+    dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
+    dev = {n: host[n].to(DEV) for n in ("Q", "K", "V", "dO")}
+    ws = dsa.alloc_bwd_det_workspace(dims, DEV)
+    det = []
+    for _ in range(2):
+        g = [torch.empty_like(out["dq"]), torch.empty_like(out["dk"]), torch.empty_like(out["dv"])]
+        dsa.sparse_attn_bwd_det(dims, dev["Q"], dev["K"], dev["V"], out["idx"], out["o"], out["lse"], dev["dO"], *g,
+                                ws, o_acc=out["o_acc"])
+        det.append(g)
+    dsa.check_device_error()
+    for a, b in zip(det[0], det[1]):
+        assert torch.equal(a, b)
+    assert torch.equal(det[0][0], out["dq"])
+    del dev, ws
     gk, gv = out["dk"].cpu().numpy(), out["dv"].cpu().numpy()
     errk, errv = np.abs(gk - dK), np.abs(gv - dV)
+    dk_det, dv_det = det[0][1].cpu().numpy(), det[0][2].cpu().numpy()
+    err_det = max(float(np.abs(dk_det - dK).max()), float(np.abs(dv_det - dV).max()))
+    del det
     counts = np.bincount(idx[idx >= 0].ravel(), minlength=wl.P)
     top = int(np.argmax(counts))
     keys = slice(4 * top, 4 * top + 4)
     rec = {"max_err_dq": eq, "max_err_dk": float(errk.max()), "max_err_dv": float(errv.max()),
            "most_selected_pool": top, "its_queries": int(counts[top]),
            "its_err_dk": float(errk[keys].max()), "its_err_dv": float(errv[keys].max()),
-           "its_max_abs_dv": float(np.abs(dV[keys]).max())}
+           "its_max_abs_dv": float(np.abs(dV[keys]).max()), "max_err_dkdv_deterministic": err_det}
     record_property("gradient_errors", rec)
     print(name, rec)
     assert eq <= 2e-2, rec
     assert errk.max() <= 2e-2 and errv.max() <= 2e-2, rec
+    assert err_det <= 2e-2, rec
 
 
 @pytest.mark.parametrize("name", ["bf16_128k_needle", "bf16_256k"])
