@@ -59,7 +59,12 @@ def load_peaks():
 # figure is reported only while the kernel's source files hash as they did
 # when it was captured; after any change to them the bench reports null until
 # it is captured again.
-TRAFFIC = {}
+TRAFFIC = {
+    ("bf16_128k_needle", "attn_bwd"): {"bytes": 11616282624 + 9580551936,
+                                       "sources": {"attn_bwd.cu": "6114a89bda28ac3a", "gather.cuh": "9c5588b13d0916cd", "common.cuh": "4c65dfd5da7caf78"}},
+    ("bf16_128k_needle", "attn_fwd"): {"bytes": 1271921920 + 1564575744,
+                                       "sources": {"attn_fwd.cu": "ffdff854d43dc7cb", "gather.cuh": "9c5588b13d0916cd", "common.cuh": "4c65dfd5da7caf78"}},
+}
 
 
 def measured_traffic(workload: str, kernel: str):
@@ -205,7 +210,9 @@ def run_ours(args, rank, world):
     dq = torch.empty((wl.L, wl.Hq, wl.d), device=dev) if with_bwd else None
     dk = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
     dv = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
-    bws = None
+    dsa.set_indexer_topk_route(args.indexer_route)
+    det = with_bwd and args.backward == "det"
+    bws = dsa.alloc_bwd_det_workspace(dims, dev) if det else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
     stream = torch.cuda.current_stream(dev)
     C = wl.q_chunk
@@ -214,8 +221,16 @@ def run_ours(args, rank, world):
     # scores when the chunk has rows of more than 2048 pools, thresholds,
     # candidates, selection, fallback scores, fallback top-k; fp32 layers: the
     # indexer and the top-k); the forward; the backward
-    per_chunk = [(5 + (((q0 + n) >> 2) > 2048)) if wl.dtype == "bf16" else 2 for q0, n in chunks]
-    launches_per_step = 1 + sum(per_chunk) + 1 + (1 if with_bwd else 0)
+    # per chunk: route 1 (and fp32 layers) the indexer and the top-k; route 0
+    # the sampled scores when a row has more than 2048 pools, thresholds,
+    # candidate indexer, selection, fallback indexer, fallback top-k
+    if wl.dtype != "bf16" or args.indexer_route == 1:
+        per_chunk = [2 for _ in chunks]
+    else:
+        per_chunk = [(1 if ((q0 + n) >> 2) > 2048 else 0) + 5 for q0, n in chunks]
+    # the deterministic backward: dQ pass, 5 inversion kernels, 3 per 4096-query band
+    bwd_launches = (1 + 5 + 3 * ((wl.L + 4095) // 4096)) if det else 1
+    launches_per_step = 1 + sum(per_chunk) + 1 + (bwd_launches if with_bwd else 0)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -240,10 +255,14 @@ def run_ours(args, rank, world):
             marks.append(("attn_fwd", timers.pop()))
             marks[-1][1].record(stream)
         if with_bwd:
-            dsa.sparse_attn_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"], dq,
-                                dk, dv, bws, None, stream, o_acc=bufs.o_acc)
+            if det:
+                dsa.sparse_attn_bwd_det(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse,
+                                        d_in["dO"], dq, dk, dv, bws, None, stream, o_acc=bufs.o_acc)
+            else:
+                dsa.sparse_attn_bwd(dims, d_in["Q"], d_in["K"], d_in["V"], bufs.idx, bufs.o, bufs.lse, d_in["dO"],
+                                    dq, dk, dv, bws, None, stream, o_acc=bufs.o_acc)
             if timers is not None:
-                marks.append(("attn_bwd", timers.pop()))
+                marks.append(("attn_bwd_det" if det else "attn_bwd", timers.pop()))
                 marks[-1][1].record(stream)
         return marks
 
@@ -295,7 +314,7 @@ def run_ours(args, rank, world):
                       "L2-flush buffer; the library allocates no device memory"}
 
     # end-to-end through the C ABI with host buffers: H2D of the inputs, the layer, D2H of the results
-    e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev)
+    e2e = end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev, det)
     clocks = clk.summary()
     return {
         "metric": METRIC if args.workload == "bf16_128k_needle" else f"DSA-layer tokens/s ({wl.passes}) {wl.name}",
@@ -304,6 +323,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "L": wl.L, "Hq": wl.Hq, "d": wl.d, "Hi": wl.Hi, "di": wl.di, "k": wl.k,
                    "q_chunk": wl.q_chunk, "pass": wl.passes, "needle": wl.needle,
+                   "indexer_topk_route": args.indexer_route, "backward": args.backward if with_bwd else None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MiB buffer written before every timed step, outside the events"},
         "roofline": rl,
@@ -340,11 +360,13 @@ def roofline(nm, alg, launch_ms, k_ms, peaks, peak_kind, wl, nchunks, ceilings=N
         if traffic is not None:
             out["hbm_frac"] = round(traffic / (ms * 1e-3) / 1e9 / hbm, 4)
         return out
-    if nm in ("attn_fwd", "attn_bwd") and ceilings and nm in ceilings:
-        c = ceilings[nm]
-        b = alg[nm]["l2_bytes"]
+    if nm in ("attn_fwd", "attn_bwd", "attn_bwd_det") and ceilings and nm.replace("_det", "") in ceilings:
+        # the deterministic backward is held to the same ceiling as the atomic
+        # one: the replay of the query-major gathers and reductions
+        c = ceilings[nm.replace("_det", "")]
+        b = alg[nm.replace("_det", "")]["l2_bytes"]
         a = b / (ms * 1e-3) / 1e9
-        fl = alg[nm]["flops"] / (ms * 1e-3) / 1e12
+        fl = alg[nm.replace("_det", "")]["flops"] / (ms * 1e-3) / 1e12
         tpk = peaks["bf16_tflops_sustained"]
         out = {"bound": "l2", "achieved": round(a, 1), "peak": round(c["gbs"], 1), "unit": "GB/s",
                "frac": round(a / c["gbs"], 4), "traffic": traffic,
@@ -402,7 +424,7 @@ def l2_ceilings(dsa, dims, wl, k, v, idx, stream, dev, with_bwd, reps=3):
     return out
 
 
-def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev):
+def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, with_bwd, world, dev, det=False):
     """Tokens/s through the public entry points with host buffers: every step
     copies its inputs in from pinned host memory, runs the layer and copies its
     outputs (O, LSE and, with a backward, dQ, dK, dV) back to pinned memory.
@@ -422,7 +444,10 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     def layer(d, o, lse, grads, s):
         dsa.layer_fwd(dims, d["Q"], d["K"], d["V"], d["q_I"], d["k_I"], d["w"], o, lse, bufs.idx, bufs.kpool,
                       bufs.ws, stream=s, o_acc=bufs.o_acc)
-        if with_bwd:
+        if det:
+            dsa.sparse_attn_bwd_det(dims, d["Q"], d["K"], d["V"], bufs.idx, o, lse, d["dO"], grads[0], grads[1],
+                                    grads[2], bws, stream=s, o_acc=bufs.o_acc)
+        elif with_bwd:
             dsa.layer_bwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o, lse, d["dO"], grads[0], grads[1], grads[2],
                           bws, stream=s, o_acc=bufs.o_acc)
 
@@ -648,6 +673,10 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10, help="end-to-end steps (at least 1; 10 by default)")
+    ap.add_argument("--indexer-route", type=int, default=1, choices=[0, 1],
+                    help="indexer + top-k route: 1 score block + row-wise top-k (default), 0 candidate lists")
+    ap.add_argument("--backward", default="atomic", choices=["atomic", "det"],
+                    help="backward: atomic (default) or the deterministic key-major one")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

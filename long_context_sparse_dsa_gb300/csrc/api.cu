@@ -41,6 +41,7 @@ namespace {
 
 thread_local char g_msg[512] = "";
 int g_indexer_topk_route = 1;   // see dsa_set_indexer_topk_route
+int g_attn_fwd_route = 1;       // see dsa_set_attn_fwd_route
 
 dsa_status fail(dsa_status st, const char* fmt, ...) {
   va_list ap;
@@ -141,7 +142,10 @@ dsa_status do_fwd(const dsa_dims* d, const void* q, const void* k, const void* v
                   float* lse, float* o_acc, cudaStream_t s) {
   cudaError_t e;
   if (is_bf16(d)) {
-    e = dsa::launch_attn_fwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, o_acc, s);
+    if (g_attn_fwd_route == 1 && dsa::attn_fwd_tc_supported(d->Hq, d->d))
+      e = dsa::launch_attn_fwd_tc_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, o_acc, s);
+    else
+      e = dsa::launch_attn_fwd_bf16(d->L, d->Hq, d->d, d->k, d->scale, q, k, v, idx, o, lse, o_acc, s);
   } else {
     e = dsa::launch_attn_fwd_f32(d->L, d->Hq, d->d, d->k, d->scale, static_cast<const float*>(q),
                                  static_cast<const float*>(k), static_cast<const float*>(v), idx,
@@ -419,6 +423,13 @@ dsa_status dsa_set_indexer_topk_route(int32_t route) {
   g_msg[0] = 0;
   if (route != 0 && route != 1) return fail(DSA_ERR_INVALID_ARG, "route must be 0 or 1");
   g_indexer_topk_route = route;
+  return DSA_OK;
+}
+
+dsa_status dsa_set_attn_fwd_route(int32_t route) {
+  g_msg[0] = 0;
+  if (route != 0 && route != 1) return fail(DSA_ERR_INVALID_ARG, "route must be 0 or 1");
+  g_attn_fwd_route = route;
   return DSA_OK;
 }
 

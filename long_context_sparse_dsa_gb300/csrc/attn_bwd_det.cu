@@ -20,7 +20,9 @@
 //      rows once and, for each query, its Q and dO rows (all heads) through a
 //      3-stage cp.async ring, recomputes S and dP, and accumulates
 //      dV^T += dO^T P and dK^T += scale Q^T dS with mma.sync (d on M, the 4
-//      keys padded to N = 8, heads on K; P and dS as bf16 hi + lo).  The
+//      keys padded to N = 8, heads on K; P and dS as bf16 hi + lo; each
+//      query's product joins the sums with fp32 adds, not inside the MMA's
+//      accumulator).  The
 //      query's own partial pool counts as a prefix of its pool's stream.  Each
 //      item writes its partial sums to its own slot;
 //   4. per band, one warp per pool adds its items' partials to dK/dV in item
@@ -219,7 +221,7 @@ struct DetCfg {
   static constexpr int ROW_BYTES = D * 2;
   static constexpr int CHUNKS = D / 8;                 // 16-byte chunks per row
   static constexpr int TILE = 16 * ROW_BYTES;          // 16 heads x D, one tensor, one head group
-  static constexpr int AUX = 2 * 16 * 4 * HG;          // LSE and D of every head
+  static constexpr int AUX = 2 * 16 * 4 * HG + 16;     // LSE and D of every head; the query and its rows
   static constexpr int STAGE = 2 * HG * TILE + AUX;    // Q and dO of all heads, LSE, D
   static constexpr int KV = 2 * 8 * ROW_BYTES;         // K and V rows of the pool (8 rows: 4 keys + zero padding)
   static constexpr int WARP_BYTES = kDetNST * STAGE + KV;
@@ -297,6 +299,14 @@ __global__ void __launch_bounds__(32 * DetCfg<D, HG>::WARPS) det_keymajor_kernel
         const int which = lane / (4 * HG), ch = lane % (4 * HG);
         cp_async16(sb + 2 * HG * C::TILE + which * 64 * HG + ch * 16, (which ? Dbuf : LSE) + t * Hq + ch * 4, 16);
       }
+      // the element's query and visible rows, for the step that consumes it
+      // (so no global load sits on that step's critical path); the stage's
+      // previous reader finished before this warp's last __syncwarp
+      if (lane == 0) {
+        int* meta = reinterpret_cast<int*>(det_smem + (sb - smem_u32(det_smem)) + 2 * HG * C::TILE + 2 * 64 * HG);
+        meta[0] = (int)t;
+        meta[1] = nr;
+      }
     };
     float accv[HG][D / 16][4], acck[HG][D / 16][4];
 #pragma unroll
@@ -316,17 +326,19 @@ __global__ void __launch_bounds__(32 * DetCfg<D, HG>::WARPS) det_keymajor_kernel
       cp_async_commit();
       cp_async_wait<2>();
       __syncwarp();
-      int64_t t;
-      int nrows;
-      elem(j, t, nrows);
       const uint32_t sb = wbase + st * C::STAGE;
       const float* aux = reinterpret_cast<const float*>(det_smem + (sb - smem_u32(det_smem)) + 2 * HG * C::TILE);
+      const int nrows = reinterpret_cast<const int*>(aux + 2 * 16 * HG)[1];
 #pragma unroll
       for (int hg = 0; hg < HG; ++hg) {
         const uint32_t qs = sb + hg * 16 * C::ROW_BYTES;                 // heads hg*16 .. +15 of Q
         const uint32_t ds = sb + HG * C::TILE + hg * 16 * C::ROW_BYTES;  // and of dO
-        // S = Q K^T and dP = dO V^T: heads x 8 keys (keys 4..7 are zero rows)
+        // S = Q K^T and dP = dO V^T: heads x 8 keys (keys 4..7 are zero rows),
+        // even and odd k-steps in two chains added at the end -- the same
+        // arithmetic as the query-major kernel, so S, P, dP and dS are the
+        // same values there and here
         float sc[4] = {0.f, 0.f, 0.f, 0.f}, dp[4] = {0.f, 0.f, 0.f, 0.f};
+        float sc2[4] = {0.f, 0.f, 0.f, 0.f}, dp2[4] = {0.f, 0.f, 0.f, 0.f};
         {
           const int arow = lane & 15, ach = lane >> 4;
           const int brow = lane & 7, bch = lane >> 3;
@@ -344,8 +356,13 @@ __global__ void __launch_bounds__(32 * DetCfg<D, HG>::WARPS) det_keymajor_kernel
             ldsm_x4(kvs + 8 * C::ROW_BYTES + brow * C::ROW_BYTES + ((chb ^ brow) << 4), vb[0], vb[1], vb[2], vb[3]);
             mma_bf16_16816(sc, a[0][0], a[0][1], a[0][2], a[0][3], kb[0], kb[1]);
             mma_bf16_16816(dp, q2[0][0], q2[0][1], q2[0][2], q2[0][3], vb[0], vb[1]);
-            mma_bf16_16816(sc, a[1][0], a[1][1], a[1][2], a[1][3], kb[2], kb[3]);
-            mma_bf16_16816(dp, q2[1][0], q2[1][1], q2[1][2], q2[1][3], vb[2], vb[3]);
+            mma_bf16_16816(sc2, a[1][0], a[1][1], a[1][2], a[1][3], kb[2], kb[3]);
+            mma_bf16_16816(dp2, q2[1][0], q2[1][1], q2[1][2], q2[1][3], vb[2], vb[3]);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[e] += sc2[e];
+            dp[e] += dp2[e];
           }
         }
         // P and dS (rows g, g+8 = heads; cols 2qi, 2qi+1 = keys)
@@ -390,10 +407,21 @@ __global__ void __launch_bounds__(32 * DetCfg<D, HG>::WARPS) det_keymajor_kernel
             uint32_t ao[4], aq[4];
             ldsm_x4_t(ds + hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4), ao[0], ao[1], ao[2], ao[3]);
             ldsm_x4_t(qs + hrow * C::ROW_BYTES + ((ch ^ (hrow & 7)) << 4), aq[0], aq[1], aq[2], aq[3]);
-            mma_bf16_16816(accv[hg][mt], ao[0], ao[1], ao[2], ao[3], pb[0][0], pb[0][1]);
-            mma_bf16_16816(acck[hg][mt], aq[0], aq[1], aq[2], aq[3], db[0][0], db[0][1]);
-            mma_bf16_16816(accv[hg][mt], ao[0], ao[1], ao[2], ao[3], pb[1][0], pb[1][1]);
-            mma_bf16_16816(acck[hg][mt], aq[0], aq[1], aq[2], aq[3], db[1][0], db[1][1]);
+            // each query's product starts from zero and joins the running
+            // sums with ordinary fp32 adds: the tensor core's own fp32
+            // accumulation does not round like an add, and over a pool's
+            // whole list (113k queries for the most-selected pool at 128k)
+            // its error builds up
+            float tv[4] = {0.f, 0.f, 0.f, 0.f}, tk[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16_16816(tv, ao[0], ao[1], ao[2], ao[3], pb[0][0], pb[0][1]);
+            mma_bf16_16816(tk, aq[0], aq[1], aq[2], aq[3], db[0][0], db[0][1]);
+            mma_bf16_16816(tv, ao[0], ao[1], ao[2], ao[3], pb[1][0], pb[1][1]);
+            mma_bf16_16816(tk, aq[0], aq[1], aq[2], aq[3], db[1][0], db[1][1]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              accv[hg][mt][c] += tv[c];
+              acck[hg][mt][c] += tk[c];
+            }
           }
         }
       }

@@ -82,6 +82,11 @@ cudaError_t launch_topk(int64_t L, int k, const float* scores, int64_t q_begin, 
 cudaError_t launch_attn_fwd_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
                                  const void* v, const int32_t* idx, void* o, float* lse, float* o_acc,
                                  cudaStream_t s);
+// tcgen05 forward (attn_fwd_tc.cu): d = 128, Hq in {16, 32}
+bool attn_fwd_tc_supported(int Hq, int d);
+cudaError_t launch_attn_fwd_tc_bf16(int64_t L, int Hq, int d, int k, float scale, const void* q, const void* kk,
+                                    const void* v, const int32_t* idx, void* o, float* lse, float* o_acc,
+                                    cudaStream_t s);
 cudaError_t launch_attn_fwd_f32(int64_t L, int Hq, int d, int k, float scale, const float* q, const float* kk,
                                 const float* v, const int32_t* idx, float* o, float* lse, cudaStream_t s);
 
