@@ -286,11 +286,12 @@ dsa_status dsa_set_indexer_topk_route(int32_t route);
 
 /* Test and measurement hook: the kernel dsa_sparse_attn_fwd (and so
  * dsa_layer_fwd) runs for bf16 layers.
- *   1 (default): for d = 128, the tcgen05 kernel: keys on the MMA's M side
- *      (128-key tiles gathered by TMA), all Hq heads on N, S^T and O^T in
- *      tensor memory; other shapes take route 0.
- *   0: the warp-level kernel (one warp per query and 16-head group,
- *      m16n8k16 MMAs, 16-key cp.async gathers).
+ *   0 (default): the warp-level kernel (one warp per query and 16-head
+ *      group, m16n8k16 MMAs, 16-key cp.async gathers).
+ *   1: for d = 128, the tcgen05 kernel: keys on the MMA's M side (128-key
+ *      tiles gathered by producer warps), all Hq heads on N, S^T and O^T in
+ *      tensor memory; other shapes take route 0.  About 3x slower at
+ *      L = 131072: with N = Hq = 16 each MMA does little work.
  * Both meet the same tolerances; they differ in summation order.  Applies to
  * calls made afterwards from any host thread.  Returns DSA_ERR_INVALID_ARG
  * for any other value. */

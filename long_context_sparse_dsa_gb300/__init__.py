@@ -81,6 +81,7 @@ def _load():
             "dsa_check_device_error": ([P], ctypes.c_int),
             "dsa_set_wait_limit": ([u32], None),
             "dsa_set_indexer_topk_route": ([i32], ctypes.c_int),
+            "dsa_set_attn_fwd_route": ([i32], ctypes.c_int),
             "dsa_selftest_bounded_wait": ([u32, P], ctypes.c_int),
             "dsa_probe_traffic": ([D, P, P, P, P, P, P], ctypes.c_int),
         }
@@ -246,8 +247,13 @@ def probe_traffic(dims, k, v, idx, dk=None, dv=None, stream=None):
 
 
 def set_indexer_topk_route(route: int):
-    """Route of the bf16 indexer + top-k: 1 score block + sampled thresholds (default), 0 candidate lists."""
+    """Route of the bf16 indexer + top-k: 1 score block + row-wise top-k (default), 0 candidate lists."""
     _check(_load().dsa_set_indexer_topk_route(int(route)), "dsa_set_indexer_topk_route")
+
+
+def set_attn_fwd_route(route: int):
+    """Kernel of the bf16 attention forward: 0 warp-level m16n8k16 (default), 1 tcgen05 (d = 128)."""
+    _check(_load().dsa_set_attn_fwd_route(int(route)), "dsa_set_attn_fwd_route")
 
 
 def set_wait_limit(spins: int):

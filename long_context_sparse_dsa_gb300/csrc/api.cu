@@ -41,7 +41,7 @@ namespace {
 
 thread_local char g_msg[512] = "";
 int g_indexer_topk_route = 1;   // see dsa_set_indexer_topk_route
-int g_attn_fwd_route = 1;       // see dsa_set_attn_fwd_route
+int g_attn_fwd_route = 0;       // see dsa_set_attn_fwd_route
 
 dsa_status fail(dsa_status st, const char* fmt, ...) {
   va_list ap;

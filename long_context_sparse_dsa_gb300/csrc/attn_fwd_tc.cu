@@ -12,13 +12,16 @@
 // Design: one persistent CTA per SM walks queries (late first); all Hq heads
 // of a query share its keys, so the heads are the N side of the MMAs and the
 // keys the M side:
-//   * a key tile is 32 pool slots = 128 keys.  One producer warp gathers it
-//     with TMA: lane i loads slot i's four K rows (and, one tile later, its
-//     four V rows) as two 4-row x 64-column boxes with the 128-byte swizzle,
-//     so the tile lands in the canonical K-major layout.  An empty or
-//     out-of-range slot loads a box outside the tensor (zero fill).  K and V
+//   * a key tile is 32 pool slots = 128 keys.  Producer warps gather it with
+//     16-byte cp.async copies (lanes along a pool's contiguous 1 KB of K or
+//     V rows) straight into the canonical K-major layout with the 128-byte
+//     swizzle; an empty or out-of-range slot is zero-filled.  The copies
+//     arrive on the stage's barrier by themselves when they land, and the MMA
+//     thread fences them into the async proxy after its wait.  (TMA box
+//     loads of the same 512-byte pieces were tried first: one producer warp
+//     issued them at about 50 cycles per box, five times too slow.)  K and V
 //     have separate stage rings: a K stage is free once S is formed, a V
-//     stage only after P.V, so most of shared memory is in flight.
+//     stage only after P.V.  Q, one contiguous box per query, comes by TMA.
 //   * one thread issues S^T = K_tile . Q^T (M = 128 keys, N = Hq, fp32 in
 //     tensor memory) and O^T += V_tile^T . P (M = 128 head dims, N = Hq; V
 //     read as an MN-major operand, P from shared memory).  O^T stays in
@@ -36,6 +39,15 @@
 //     in fp32 at the end.
 // Every wait is bounded; on expiry the CTA records a timeout and unwinds,
 // waiting for its own copies and MMAs before it frees tensor memory.
+//
+// Measured against the warp-level kernel (attn_fwd.cu) at L = 131072, Hq = 16,
+// k = 512: 33.3 ms against 10.2 ms with o_acc, 28.1 against 8.2 without.  A
+// clock64 breakdown shows the gather keeping up and the MMA thread busy
+// ~2,500 cycles per 128-key tile: an M=128, N=16, K=16 MMA occupies the
+// tensor pipe for about 88 cycles (8 more MMAs per tile with o_acc cost 5.2
+// ms), roughly 9% of its dense rate, and a tile needs 16 to 24 of them.  Only
+// the Hq heads of one query share its keys, so N cannot grow; the warp-level
+// kernel stays the default and this one is the alternative route.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -52,7 +64,8 @@ struct FtcCfg {
   static constexpr int CB = TK * 128;             // one 64-column block of a K or V tile
   static constexpr int KV_TILE = 2 * CB;          // 32 KB
   static constexpr int NKS = 3;                   // K stages
-  static constexpr int NVS = HQ == 16 ? 3 : 2;    // V stages
+  static constexpr int NVS = 3;                   // V stages
+  static constexpr int NPB = HQ == 16 ? 2 : 1;    // P buffers
   static constexpr int Q_CB = HQ * 128;           // one 64-column block of the Q tile
   static constexpr int Q_TILE = 2 * Q_CB;
   static constexpr int P_CB = HQ * 128;           // 64 keys of P^T (rows = heads)
@@ -62,7 +75,7 @@ struct FtcCfg {
   static constexpr int OFF_V = OFF_K + NKS * KV_TILE;
   static constexpr int OFF_Q = OFF_V + NVS * KV_TILE;
   static constexpr int OFF_P = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_PART = OFF_P + 2 * P_BUF;     // [4][HQ] fp32: partial-pool scores
+  static constexpr int OFF_PART = OFF_P + NPB * P_BUF;   // [4][HQ] fp32: partial-pool scores
   static constexpr int OFF_RED = OFF_PART + 4 * HQ * 4;  // [4][HQ] fp32: tile maxima per warp
   static constexpr int OFF_SUM = OFF_RED + 4 * HQ * 4;   // [4][HQ] fp32: row sums per warp
   static constexpr int OFF_BAR = OFF_SUM + 4 * HQ * 4;
@@ -70,7 +83,11 @@ struct FtcCfg {
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;   // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
   static constexpr int TMEM_COLS = 4 * HQ;        // S^T x2, O^T x2
-  static constexpr int THREADS = 192;             // softmax warps 0-3, MMA warp 4, producer warp 5
+  // producer warps: four at 16 heads; two at 32 (seven warps leave the
+  // softmax threads 255 registers for their 3 x 32 per-head values)
+  static constexpr int NPW = HQ == 16 ? 4 : 2;
+  static constexpr int SPW = SLOTS / NPW;         // pool slots per producer warp and tile
+  static constexpr int THREADS = 32 * (5 + NPW);  // softmax warps 0-3, MMA warp 4, producers 5..
   static constexpr int TPH = 128 / HQ;            // partial pool: threads per head
   static constexpr int EPT = D / TPH;             // partial pool: elements per thread
 };
@@ -82,6 +99,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "[%2];\n" ::"r"(dst),
       "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
@@ -151,8 +173,7 @@ struct FtcArgs {
 
 template <int HQ, bool ACC>
 __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                       const __grid_constant__ CUtensorMap tmap_q, const FtcArgs a) {
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const FtcArgs a) {
   using C = FtcCfg<HQ>;
   constexpr float kLazy = 8.f;   // the base lags the running max by at most this (log2 units)
   extern __shared__ unsigned char smem_raw[];
@@ -191,11 +212,11 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NKS; ++s) {
-      mbar_init(kfull(s), 1);
+      mbar_init(kfull(s), 32 * C::NPW);   // every producer thread
       mbar_init(kfree(s), 1);
     }
     for (int s = 0; s < C::NVS; ++s) {
-      mbar_init(vfull(s), 1);
+      mbar_init(vfull(s), 32 * C::NPW);
       mbar_init(vfree(s), 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -211,8 +232,6 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
     prefetch_tmap(&tmap_q);
   }
   if (warp == 4) {
@@ -224,94 +243,118 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 5) {
-    // ------------------------------------------------------------ TMA producer
-    // Lane i gathers pool slot i of each tile.  V of tile g is issued after K
-    // of tile g+1: V is needed one softmax later than K.
-    uint32_t gk = 0, gv = 0, nq = 0, nqi = 0;   // nqi: Q tiles issued
-    int32_t prev_y = -4;
-    bool have_prev = false, ok = true, bad = false;
-    auto issue_v = [&](int32_t y) -> bool {
-      const int s = gv % C::NVS;
-      bool w = true;
-      if (lane == 0) {
-        w = mbar_wait(vfree(s), ((gv / C::NVS) & 1) ^ 1, abort_flag);
-        if (w) mbar_arrive_expect_tx(vfull(s), C::KV_TILE);
+  if (warp >= 5) {
+    // ---------------------------------------------------- cp.async producers
+    // Producer warp pw gathers pool slots SPW*pw .. SPW*pw+SPW-1 of every
+    // tile: per slot two 16-byte copies per lane for K (rows 2u, 2u+1, lanes
+    // along the 256-byte rows) and two for V, written straight into the
+    // swizzled canonical layout.  V of tile g goes out after K of tile g+1 (V
+    // is needed one softmax later).  Each thread's copies of a stage arrive on
+    // the stage's full barrier by themselves when they land
+    // (cp.async.mbarrier.arrive.noinc), so a producer only ever waits for a
+    // free stage; the MMA thread fences them into the async proxy.
+    const int pw = warp - 5;
+    const int rlo = lane >> 4, j16 = lane & 15, cblk = j16 >> 3, jj = j16 & 7;
+    const uint32_t src_off = (uint32_t)(rlo * 256 + j16 * 16);
+    uint32_t dst_off[2][2];   // [slot parity][copy]
+#pragma unroll
+    for (int par = 0; par < 2; ++par)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = 2 * u + rlo;
+        dst_off[par][u] = (uint32_t)(cblk * C::CB + r * 128 + ((jj ^ (4 * par + r)) << 4));
       }
-      if (!__shfl_sync(0xffffffffu, (int)w, 0)) return false;
-      const uint32_t dst = sV + s * C::KV_TILE + lane * 512;
-      tma_load_2d(dst, &tmap_v, vfull(s), 0, y);
-      tma_load_2d(dst + C::CB, &tmap_v, vfull(s), 64, y);
-      ++gv;
-      return true;
+    const char* Kb = reinterpret_cast<const char*>(a.K);
+    const char* Vb = reinterpret_cast<const char*>(a.V);
+    uint32_t g = 0;   // tiles issued
+    bool ok = true, bad = false;
+    // copies of one tensor's SPW slots of a tile into `stage`; `mine` is the
+    // pool of slot SPW*pw + lane (lanes 0..SPW-1), -1 for none
+    auto gather = [&](const char* base, uint32_t stage, int mine) {
+#pragma unroll
+      for (int i = 0; i < C::SPW; ++i) {
+        const int pool = __shfl_sync(0xffffffffu, mine, i);
+        const uint32_t bytes = pool >= 0 ? 16u : 0u;
+        const char* src = base + (int64_t)(pool >= 0 ? pool : 0) * 1024 + src_off;
+        const uint32_t dst = stage + (uint32_t)(C::SPW * pw + i) * 512u;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) cp_async16(dst + dst_off[i & 1][u], src + u * 512, bytes);
+      }
     };
-    for (int64_t i = blockIdx.x; ok && i < L; i += gridDim.x, ++nq) {
+    auto wait_free = [&](uint32_t bar, uint32_t parity) -> bool {
+      bool w = true;
+      if (lane == 0) w = mbar_wait(bar, parity, abort_flag);
+      return __shfl_sync(0xffffffffu, (int)w, 0) != 0;
+    };
+    int pool_prev = -1;   // this lane's slot of the previous tile (for its V)
+    for (int64_t i = blockIdx.x; ok && i < L; i += gridDim.x) {
       const int64_t t = L - 1 - i;
-      const int qb = nq & 1;
-      {
-        bool w = true;
-        if (lane == 0) {
-          w = mbar_wait(qfree(qb), ((nq >> 1) & 1) ^ 1, abort_flag);
-          if (w) {
-            mbar_arrive_expect_tx(qfull(qb), C::Q_TILE);
-            tma_load_3d(sQ + qb * C::Q_TILE, &tmap_q, qfull(qb), 0, 0, (int32_t)t);
-            tma_load_3d(sQ + qb * C::Q_TILE + C::Q_CB, &tmap_q, qfull(qb), 64, 0, (int32_t)t);
-          }
-        }
-        nqi += w ? 1u : 0u;
-        if (!(ok = __shfl_sync(0xffffffffu, (int)w, 0) != 0)) break;
-      }
       const int64_t el = elig(t);
       const int32_t* irow = a.idx + t * (int64_t)k;
-      for (int j = 0; j < T; ++j) {
-        const int slot = j * C::SLOTS + lane;
+      auto pool_of = [&](int j) -> int {   // this lane's slot of tile j of this query
+        const int slot = j * C::SLOTS + C::SPW * pw + (lane & (C::SPW - 1));
         const int p = slot < k ? __ldg(irow + slot) : -1;
         bad |= p >= el;
-        const int32_t y = (p >= 0 && p < el) ? 4 * p : -4;   // -4: a box wholly outside the tensor
-        const int s = gk % C::NKS;
-        bool w = true;
-        if (lane == 0) {
-          w = mbar_wait(kfree(s), ((gk / C::NKS) & 1) ^ 1, abort_flag);
-          if (w) mbar_arrive_expect_tx(kfull(s), C::KV_TILE);
+        return (p >= 0 && p < el) ? p : -1;
+      };
+      int pool_next = pool_of(0);
+      for (int j = 0; j < T; ++j) {
+        const int pool_cur = pool_next;
+        if (j + 1 < T) pool_next = pool_of(j + 1);   // a tile ahead of its use
+        const int ks = g % C::NKS;
+        if (!(ok = wait_free(kfree(ks), ((g / C::NKS) & 1) ^ 1))) break;
+        gather(Kb, sK + ks * C::KV_TILE, pool_cur);
+        cp_async_arrive_noinc(kfull(ks));
+        if (g >= 1) {
+          const int vs = (g - 1) % C::NVS;
+          if (!(ok = wait_free(vfree(vs), (((g - 1) / C::NVS) & 1) ^ 1))) break;
+          gather(Vb, sV + vs * C::KV_TILE, pool_prev);
+          cp_async_arrive_noinc(vfull(vs));
         }
-        if (!(ok = __shfl_sync(0xffffffffu, (int)w, 0) != 0)) break;
-        const uint32_t dst = sK + s * C::KV_TILE + lane * 512;
-        tma_load_2d(dst, &tmap_k, kfull(s), 0, y);
-        tma_load_2d(dst + C::CB, &tmap_k, kfull(s), 64, y);
-        ++gk;
-        if (have_prev && !(ok = issue_v(prev_y))) break;
-        prev_y = y;
-        have_prev = true;
+        pool_prev = pool_cur;
+        ++g;
       }
     }
-    if (ok && have_prev) ok = issue_v(prev_y);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
-    // On abort, wait (bounded) for the loads issued last into each buffer, so
-    // no TMA write lands after the CTA has exited.
-    if (!ok && lane == 0) {
-      *abort_flag = 1;
-      for (uint32_t g = (gk > (uint32_t)C::NKS ? gk - C::NKS : 0); g < gk; ++g)
-        mbar_wait(kfull(g % C::NKS), (g / C::NKS) & 1, nullptr);
-      for (uint32_t g = (gv > (uint32_t)C::NVS ? gv - C::NVS : 0); g < gv; ++g)
-        mbar_wait(vfull(g % C::NVS), (g / C::NVS) & 1, nullptr);
-      for (uint32_t g = (nqi > 2u ? nqi - 2 : 0); g < nqi; ++g) mbar_wait(qfull(g & 1), (g >> 1) & 1, nullptr);
+    if (ok && g >= 1) {
+      const int vs = (g - 1) % C::NVS;
+      if ((ok = wait_free(vfree(vs), (((g - 1) / C::NVS) & 1) ^ 1))) {
+        gather(Vb, sV + vs * C::KV_TILE, pool_prev);
+        cp_async_arrive_noinc(vfull(vs));
+      }
     }
+    // every copy of this thread has landed before the CTA can exit
+    cp_async_commit();
+    cp_async_wait<0>();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(DSA_DEV_ERR_BAD_INDEX);
+    if (!ok) *abort_flag = 1;
   } else if (warp == 4) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(C::TK, HQ);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(C::D, HQ) | (1u << 15);   // A (V^T) MN-major
-      uint32_t gk = 0, gp = 0, nq = 0;
+      uint32_t gk = 0, gp = 0, nq = 0, nqi = 0;   // nqi: Q tiles issued
       bool ok = true;
+      // Q tile of the CTA's n-th query (row t) into buffer n & 1, once the
+      // S MMAs of query n-2 have finished reading that buffer
+      auto load_q = [&](uint32_t n, int64_t t) -> bool {
+        if (!mbar_wait(qfree(n & 1), ((n >> 1) & 1) ^ 1, abort_flag)) return false;
+        mbar_arrive_expect_tx(qfull(n & 1), C::Q_TILE);
+        tma_load_3d(sQ + (n & 1) * C::Q_TILE, &tmap_q, qfull(n & 1), 0, 0, (int32_t)t);
+        tma_load_3d(sQ + (n & 1) * C::Q_TILE + C::Q_CB, &tmap_q, qfull(n & 1), 64, 0, (int32_t)t);
+        ++nqi;
+        return true;
+      };
+      if (blockIdx.x < L) ok = load_q(0, L - 1 - (int64_t)blockIdx.x);
       // O^T += V^T P for tile gp (the first tile of a query starts the accumulator)
       auto pv = [&](bool first) -> bool {
-        const int vs = gp % C::NVS, pb = gp & 1, ob = nq & 1;
+        const int vs = gp % C::NVS, pb = gp & 1, ob = nq & 1;   // pb: pfull/pvdone barrier
         if (!mbar_wait(vfull(vs), (gp / C::NVS) & 1, abort_flag)) return false;
         if (!mbar_wait(pfull(pb), (gp >> 1) & 1, abort_flag)) return false;
         if (first && !mbar_wait(ofree(ob), ((nq >> 1) & 1) ^ 1, abort_flag)) return false;
+        fence_proxy_async_shared();   // the producers' copies, seen through the barrier
         tc_fence_after();
         const uint32_t d_o = tmem_base + 2 * HQ + ob * HQ;
-        const uint32_t vt = sV + vs * C::KV_TILE, pt = sP + pb * C::P_BUF;
+        const uint32_t vt = sV + vs * C::KV_TILE, pt = sP + (gp % C::NPB) * C::P_BUF;
 #pragma unroll
         for (int kk = 0; kk < C::TK / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128_mn(vt + kk * 16 * 128, C::CB, 1024);
@@ -338,6 +381,7 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
           const int s = gk % C::NKS, sb = gk & 1;
           if (!(ok = mbar_wait(kfull(s), (gk / C::NKS) & 1, abort_flag))) break;
           if (!(ok = mbar_wait(sfree(sb), ((gk >> 1) & 1) ^ 1, abort_flag))) break;
+          fence_proxy_async_shared();   // the producers' copies, seen through the barrier
           tc_fence_after();
           const uint32_t kt = sK + s * C::KV_TILE, qt = sQ + qb * C::Q_TILE;
 #pragma unroll
@@ -348,15 +392,23 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
           }
           tc_commit(kfree(s));
           tc_commit(sfull(sb));
-          if (j == T - 1) tc_commit(qfree(qb));
           ++gk;
+          if (j == T - 1) {
+            tc_commit(qfree(qb));
+            const int64_t inext = i + gridDim.x;
+            if (inext < L && !(ok = load_q(nq + 1, L - 1 - inext))) break;
+          }
           if (j >= 1 && !(ok = pv(j == 1))) break;
         }
         if (!ok) break;
         if (!(ok = pv(T == 1))) break;
         tc_commit(ofull(nq & 1));
       }
-      if (!ok) *abort_flag = 1;
+      if (!ok) {
+        *abort_flag = 1;
+        // no TMA write may land after the CTA has exited
+        for (uint32_t n = (nqi > 2u ? nqi - 2 : 0); n < nqi; ++n) mbar_wait(qfull(n & 1), (n >> 1) & 1, nullptr);
+      }
       // Drain: every MMA this thread issued has finished before TMEM is freed.
       tc_commit(drain_bar);
       mbar_wait(drain_bar, 0, nullptr);
@@ -485,9 +537,11 @@ __global__ void __launch_bounds__(FtcCfg<HQ>::THREADS, 1)
             tmem_st_wait();
           }
         }
-        // the P buffer of this tile was last read by P.V two tiles ago
-        if (gk >= 2) ok &= mbar_wait(pvdone(sb), ((gk - 2) >> 1) & 1, abort_flag);
-        const uint32_t pt = sP + sb * C::P_BUF + (key >> 6) * C::P_CB + (((key & 63) >> 3) << 4) + (key & 7) * 2;
+        // the P buffer of this tile was last read by P.V NPB tiles ago
+        if (gk >= (uint32_t)C::NPB)
+          ok &= mbar_wait(pvdone((gk - C::NPB) & 1), ((gk - C::NPB) >> 1) & 1, abort_flag);
+        const uint32_t pt =
+            sP + (gk % C::NPB) * C::P_BUF + (key >> 6) * C::P_CB + (((key & 63) >> 3) << 4) + (key & 7) * 2;
 #pragma unroll
         for (int h = 0; h < HQ; ++h) {
           const float bh = base[h] == -INFINITY ? 0.f : base[h];
@@ -584,22 +638,8 @@ static cudaError_t launch_ftc(const FtcArgs& a, cudaStream_t s) {
   using C = FtcCfg<HQ>;
   auto enc = ftc_encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap tk, tv, tq;
+  CUtensorMap tq;
   const cuuint32_t estr[3] = {1, 1, 1};
-  {
-    // K and V: [L rows, 128 columns]; a box is 4 rows (one pool) x 64 columns
-    const cuuint64_t dims[2] = {(cuuint64_t)C::D, (cuuint64_t)a.L};
-    const cuuint64_t strides[1] = {(cuuint64_t)C::D * 2};
-    const cuuint32_t box[2] = {64, 4};
-    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.K), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-    if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.V), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
   {
     // Q: [L, HQ, 128]; a box is one query's HQ heads x 64 columns
     const cuuint64_t dims[3] = {(cuuint64_t)C::D, (cuuint64_t)HQ, (cuuint64_t)a.L};
@@ -615,7 +655,7 @@ static cudaError_t launch_ftc(const FtcArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int64_t grid = device_sm_count();
   if (grid > a.L) grid = a.L;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tk, tv, tq, a);
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, s>>>(tq, a);
   return cudaGetLastError();
 }
 

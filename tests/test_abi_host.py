@@ -182,3 +182,13 @@ def test_binding_has_no_cpu_path():
     import inspect
     src = inspect.getsource(dsa)
     assert "oracle" not in src and "numpy" not in src
+
+
+def test_route_setters_accept_only_their_routes(lib):
+    """The two route hooks take 0 or 1 and nothing else; they only set a host
+    variable (nothing is launched), and are left at their documented defaults
+    (indexer + top-k: 1, attention forward: 0)."""
+    for setter, default in ((lib.dsa_set_indexer_topk_route, 1), (lib.dsa_set_attn_fwd_route, 0)):
+        assert setter(2) == 1 and setter(-1) == 1          # DSA_ERR_INVALID_ARG
+        assert setter(0) == 0 and setter(1) == 0
+        assert setter(default) == 0

@@ -298,10 +298,19 @@ def _attn_case(L, Hq, d, k, dtype, seed):
     return Q, K, V, dO, idx
 
 
+@pytest.fixture(params=[1, 0], ids=["tcgen05", "warp"])
+def fwd_route(request):
+    """Run the test under each bf16 forward kernel (d = 64 always takes the
+    warp-level one); the library default (0) is restored afterwards."""
+    dsa.set_attn_fwd_route(request.param)
+    yield request.param
+    dsa.set_attn_fwd_route(0)
+
+
 @pytest.mark.parametrize("dtype,Hq,d", [("bf16", 16, 128), ("bf16", 32, 128), ("bf16", 16, 64), ("fp32", 8, 64),
                                         ("fp32", 5, 128)])
 @pytest.mark.parametrize("k", [1, 5, 32])
-def test_attn_fwd_matches_oracle(dtype, Hq, d, k):
+def test_attn_fwd_matches_oracle(dtype, Hq, d, k, fwd_route):
     L = 1000
     Q, K, V, _, idx = _attn_case(L, Hq, d, k, dtype, seed=10 + k)
     scale = 1 / math.sqrt(d)
@@ -324,6 +333,54 @@ def test_attn_fwd_matches_oracle(dtype, Hq, d, k):
     assert np.abs(o_acc.cpu().numpy() - Or).max() <= 1e-4
     if dtype == "fp32":
         assert torch.equal(O2, O) and torch.equal(o_acc, O)
+
+
+@pytest.mark.parametrize("Hq", [16, 32])
+@pytest.mark.parametrize("spiky", [False, True])
+def test_attn_fwd_tc_many_tiles_and_queries(Hq, spiky):
+    """The tcgen05 forward at L = 8192, k = 512: 16 key tiles per query and
+    tens of queries per persistent CTA, so every stage ring, accumulator and
+    barrier phase wraps many times.  `spiky` scales Q by 6, so the scores
+    span ~2^9 and the softmax base moves (rescaling O in tensor memory) on
+    many tiles.  Sampled rows (the first 40, whose selections are padded with
+    -1, and a spread of later ones) against the oracle, with and without
+    o_acc; every row against the warp-level kernel."""
+    L, d, k = 8192, 128, 512
+    Q, K, V, _, idx = _attn_case(L, Hq, d, k, "bf16", seed=90 + Hq)
+    if spiky:
+        Q = (Q.float() * 6).to(torch.bfloat16)
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale, dtype="bf16")
+    dev = [t.to(DEV) for t in (Q, K, V)]
+    idx_d = torch.from_numpy(idx).to(DEV)
+    out = {}
+    try:
+        for route in (1, 0):
+            dsa.set_attn_fwd_route(route)
+            O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+            lse = torch.empty((L, Hq), device=DEV)
+            o_acc = torch.full((L, Hq, d), float("nan"), device=DEV)
+            dsa.sparse_attn_fwd(dims, *dev, idx_d, O, lse, o_acc=o_acc)
+            O2 = torch.empty_like(O)
+            lse2 = torch.empty_like(lse)
+            dsa.sparse_attn_fwd(dims, *dev, idx_d, O2, lse2)
+            dsa.check_device_error()
+            out[route] = (O, lse, o_acc, O2, lse2)
+    finally:
+        dsa.set_attn_fwd_route(0)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([np.arange(40), rng.integers(40, L, 88), [L - 4, L - 3, L - 2, L - 1]]))
+    Or, LSEr = oracle.attn_fwd(_f32(Q), _f32(K), _f32(V), idx, scale, rows=rows)
+    O, lse, o_acc, O2, lse2 = out[1]
+    assert torch.equal(lse2, lse)
+    assert np.abs(_f32(O)[rows] - Or).max() <= 2e-2
+    assert np.abs(_f32(O2)[rows] - Or).max() <= 2e-2
+    assert np.abs(lse.cpu().numpy()[rows] - LSEr).max() <= 1e-3
+    assert np.abs(o_acc.cpu().numpy()[rows] - Or).max() <= 1e-4
+    Ow, lsew, accw, _, _ = out[0]
+    assert (O.float() - Ow.float()).abs().max().item() <= 2e-2
+    assert (lse - lsew).abs().max().item() <= 1e-4
+    assert (o_acc - accw).abs().max().item() <= 1e-4
 
 
 def _bwd(det, dims, dev, idx_d, O, lse, dq, dk, dv, o_acc):
@@ -448,7 +505,7 @@ def test_attn_bwd_scaled_inputs(case, use_o_acc, det):
         assert np.abs(g).max() >= 0.5 * np.abs(ref).max(), name
 
 
-def test_attn_bad_index_is_skipped_and_reported():
+def test_attn_bad_index_is_skipped_and_reported(fwd_route):
     L, Hq, d, k = 256, 16, 128, 4
     Q, K, V, _, idx = _attn_case(L, Hq, d, k, "bf16", seed=5)
     idx = idx.copy()
