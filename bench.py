@@ -64,6 +64,11 @@ TRAFFIC = {
                                        "sources": {"attn_bwd.cu": "6114a89bda28ac3a", "gather.cuh": "9c5588b13d0916cd", "common.cuh": "4c65dfd5da7caf78"}},
     ("bf16_128k_needle", "attn_fwd"): {"bytes": 1271921920 + 1564575744,
                                        "sources": {"attn_fwd.cu": "ffdff854d43dc7cb", "gather.cuh": "9c5588b13d0916cd", "common.cuh": "4c65dfd5da7caf78"}},
+    # mean over the 16 chunk launches of one step
+    ("bf16_128k_needle", "indexer"): {"bytes": 37685632 + 480333056,
+                                      "sources": {"indexer_tc.cu": "6267c910c1505ced", "common.cuh": "4c65dfd5da7caf78"}},
+    ("bf16_128k_needle", "topk"): {"bytes": 538221632 + 11386624,
+                                   "sources": {"topk.cu": "3a87db186862256b", "common.cuh": "4c65dfd5da7caf78"}},
 }
 
 
@@ -211,6 +216,7 @@ def run_ours(args, rank, world):
     dk = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
     dv = torch.empty((wl.L, wl.d), device=dev) if with_bwd else None
     dsa.set_indexer_topk_route(args.indexer_route)
+    dsa.set_attn_fwd_route(args.attn_fwd_route)
     det = with_bwd and args.backward == "det"
     bws = dsa.alloc_bwd_det_workspace(dims, dev) if det else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MiB > L2
@@ -232,6 +238,9 @@ def run_ours(args, rank, world):
     bwd_launches = (1 + 5 + 3 * ((wl.L + 4095) // 4096)) if det else 1
     launches_per_step = 1 + sum(per_chunk) + 1 + (bwd_launches if with_bwd else 0)
 
+    split_pair = args.indexer_route == 1 or wl.dtype != "bf16"
+    scores = bufs.ws.view(torch.float32)   # the score block of route 1 (the workspace holds it)
+
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
@@ -245,6 +254,19 @@ def run_ours(args, rank, world):
             marks.append(("pool_keys", timers.pop()))
             marks[-1][1].record(stream)
         for q0, n in chunks:
+            if split_pair:
+                # route 1 is the indexer's score block and the row-wise top-k:
+                # the same two kernels through their own entry points, so that
+                # each gets its own time and roofline
+                dsa.indexer_score(dims, d_in["q_I"], bufs.kpool, d_in["w"], q0, n, scores, stream=stream)
+                if timers is not None:
+                    marks.append(("indexer", timers.pop()))
+                    marks[-1][1].record(stream)
+                dsa.topk(dims, scores, q0, n, bufs.idx, stream=stream)
+                if timers is not None:
+                    marks.append(("topk", timers.pop()))
+                    marks[-1][1].record(stream)
+                continue
             dsa.indexer_topk(dims, d_in["q_I"], bufs.kpool, d_in["w"], q0, n, bufs.idx, bufs.ws, stream=stream)
             if timers is not None:
                 marks.append(("indexer_topk", timers.pop()))
@@ -273,7 +295,7 @@ def run_ours(args, rank, world):
 
     per_kernel = {}
     step_ms = []
-    n_marks = 2 + len(chunks) + 2 + 1
+    n_marks = 2 + 2 * len(chunks) + 2 + 1
     with ClockSampler(local) as clk:
         if world > 1:
             torch.distributed.barrier()
@@ -323,7 +345,8 @@ def run_ours(args, rank, world):
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "L": wl.L, "Hq": wl.Hq, "d": wl.d, "Hi": wl.Hi, "di": wl.di, "k": wl.k,
                    "q_chunk": wl.q_chunk, "pass": wl.passes, "needle": wl.needle,
-                   "indexer_topk_route": args.indexer_route, "backward": args.backward if with_bwd else None,
+                   "indexer_topk_route": args.indexer_route, "attn_fwd_route": args.attn_fwd_route,
+                   "backward": args.backward if with_bwd else None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MiB buffer written before every timed step, outside the events"},
         "roofline": rl,
@@ -677,6 +700,8 @@ def main():
                     help="indexer + top-k route: 1 score block + row-wise top-k (default), 0 candidate lists")
     ap.add_argument("--backward", default="atomic", choices=["atomic", "det"],
                     help="backward: atomic (default) or the deterministic key-major one")
+    ap.add_argument("--attn-fwd-route", type=int, default=0, choices=[0, 1],
+                    help="attention forward: 0 warp-level kernel (default), 1 tcgen05 kernel")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
