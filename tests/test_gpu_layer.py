@@ -12,7 +12,9 @@
   every row, dK and dV included (the oracle sharded over the host's cores, on
   the GPU's own selection);
 * integer twins of the 128k-needle and 256k workloads: the selection bit for
-  bit on sampled rows of 32768 and 65536 pools.
+  bit on sampled rows of 32768 and 65536 pools;
+* the tcgen05 forward (route 1) at full size against the warp-level forward on
+  every row and against the oracle on sampled rows.
 """
 import math
 import os
@@ -286,3 +288,43 @@ def test_full_size_integer_twin_selection_bitexact(name):
     ref = oracle.select_rows(f["q_I"], kp, f["w"], wl.k, rows, threads=NTHREADS, block=32)
     bad = np.nonzero(~np.all(got == ref, axis=1))[0]
     assert bad.size == 0, rows[bad[:5]]
+
+
+@pytest.mark.parametrize("name", ["bf16_128k_needle", "bf16_256k"])
+def test_full_size_tcgen05_forward(name):
+    """The tcgen05 forward (route 1) at full size, on the layer's own selection:
+    every row against the warp-level forward (route 0) -- O within 2e-2, LSE
+    within 1e-4, o_acc within 1e-4 -- and sampled rows (early padded rows,
+    needle rows and a spread of the rest) against the oracle."""
+    wl = dsa_inputs.WORKLOADS[name]
+    host = dsa_inputs.make(wl, ("Q", "K", "V", "q_I", "k_I", "w"))
+    dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
+    dev = {n: t.to(DEV) for n, t in host.items()}
+    bufs = dsa.alloc_forward_buffers(dims, DEV, o_acc=True)
+    outs = {}
+    try:
+        for route in (0, 1):
+            dsa.set_attn_fwd_route(route)
+            if route == 0:
+                dsa.layer_fwd(dims, dev["Q"], dev["K"], dev["V"], dev["q_I"], dev["k_I"], dev["w"], bufs.o, bufs.lse,
+                              bufs.idx, bufs.kpool, bufs.ws, o_acc=bufs.o_acc)
+                outs[0] = (bufs.o, bufs.lse, bufs.o_acc)
+            else:
+                o, lse, acc = torch.empty_like(bufs.o), torch.empty_like(bufs.lse), torch.empty_like(bufs.o_acc)
+                dsa.sparse_attn_fwd(dims, dev["Q"], dev["K"], dev["V"], bufs.idx, o, lse, o_acc=acc)
+                outs[1] = (o, lse, acc)
+            dsa.check_device_error()
+    finally:
+        dsa.set_attn_fwd_route(0)
+    (o0, l0, a0), (o1, l1, a1) = outs[0], outs[1]
+    assert (o1.float() - o0.float()).abs().max().item() <= 2e-2
+    assert (l1 - l0).abs().max().item() <= 1e-4
+    assert (a1 - a0).abs().max().item() <= 1e-4
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([np.arange(0, 12), rng.integers(12, wl.L, 48), [wl.L - 1]]))
+    idx = bufs.idx.cpu().numpy()
+    Qr = _f32(host["Q"][torch.from_numpy(rows)])   # only the sampled rows of Q
+    O, LSE = oracle.attn_fwd(Qr, _f32(host["K"]), _f32(host["V"]), idx, wl.scale, rows=rows, q_compact=True)
+    assert np.abs(_f32(o1)[rows] - O).max() <= 2e-2
+    assert np.abs(a1.cpu().numpy()[rows] - O).max() <= 1e-4
+    assert np.abs(l1.cpu().numpy()[rows] - LSE).max() <= 1e-3
