@@ -432,7 +432,7 @@ def test_attn_bwd_det_matches_oracle_and_repeats(Hq, d, k, use_o_acc):
     assert max(errs.values()) <= 2e-2, errs
 
 
-@pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64)])
+@pytest.mark.parametrize("Hq,d", [(16, 128), (32, 128), (16, 64), (32, 64)])
 @pytest.mark.parametrize("k", [3, 32])
 @pytest.mark.parametrize("use_o_acc", [False, True])
 def test_attn_bwd_matches_oracle(Hq, d, k, use_o_acc):
@@ -523,3 +523,30 @@ def test_attn_bad_index_is_skipped_and_reported(fwd_route):
     clean[100, 1] = -1
     Or, _ = oracle.attn_fwd(_f32(Q), _f32(K), _f32(V), clean, 1 / math.sqrt(d), rows=[100, 200])
     assert np.abs(_f32(O)[[100, 200]] - Or).max() <= 2e-2
+
+
+@pytest.mark.parametrize("use_o_acc", [False, True])
+def test_attn_bwd_two_head_groups_long_rows(use_o_acc):
+    """Hq = 32: the two 16-head groups of a query are a warp pair that sums its
+    dK/dV tiles before one reduction per key.  L = 4096 with k = 256 gives rows
+    of up to 65 key steps (so the pair's barriers and shared stages cycle many
+    times), compared element by element with the oracle."""
+    L, Hq, d, k = 4096, 32, 128, 256
+    Q, K, V, dO, idx = _attn_case(L, Hq, d, k, "bf16", seed=77)
+    scale = 1 / math.sqrt(d)
+    dims = dsa.make_dims(L, Hq, d, 8, 64, k, scale=scale, dtype="bf16")
+    dev = [t.to(DEV) for t in (Q, K, V, dO)]
+    idx_d = torch.from_numpy(idx).to(DEV)
+    O = torch.empty((L, Hq, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((L, Hq), device=DEV)
+    o_acc = torch.empty((L, Hq, d), device=DEV) if use_o_acc else None
+    dsa.sparse_attn_fwd(dims, dev[0], dev[1], dev[2], idx_d, O, lse, o_acc=o_acc)
+    dq = torch.empty((L, Hq, d), device=DEV)
+    dk = torch.empty((L, d), device=DEV)
+    dv = torch.empty((L, d), device=DEV)
+    _bwd(False, dims, dev, idx_d, O, lse, dq, dk, dv, o_acc)
+    dsa.check_device_error()
+    dQr, dKr, dVr = oracle.attn_bwd(_f32(Q), _f32(K), _f32(V), idx, _f32(dO), scale, threads=8)
+    errs = {name: float(np.abs(got.cpu().numpy() - ref).max())
+            for name, got, ref in (("dQ", dq, dQr), ("dK", dk, dKr), ("dV", dv, dVr))}
+    assert max(errs.values()) <= 2e-2, errs
