@@ -43,11 +43,13 @@
 // Measured against the warp-level kernel (attn_fwd.cu) at L = 131072, Hq = 16,
 // k = 512: 33.3 ms against 10.2 ms with o_acc, 28.1 against 8.2 without.  A
 // clock64 breakdown shows the gather keeping up and the MMA thread busy
-// ~2,500 cycles per 128-key tile: an M=128, N=16, K=16 MMA occupies the
-// tensor pipe for about 88 cycles (8 more MMAs per tile with o_acc cost 5.2
-// ms), roughly 9% of its dense rate, and a tile needs 16 to 24 of them.  Only
-// the Hq heads of one query share its keys, so N cannot grow; the warp-level
-// kernel stays the default and this one is the alternative route.
+// issuing: a one-thread loop of back-to-back M = 128, K = 16 bf16 MMAs takes
+// 189 cycles per MMA whatever N is (16 to 256) and however many independent
+// accumulators it cycles through, so an N = 16 MMA does 1/16 of the work of
+// an N = 256 one in the same time.  A tile needs 16 to 24 of them (8 more
+// with o_acc cost 5.2 ms in this kernel).  Only the Hq heads of one query
+// share its keys, so N cannot grow; the warp-level kernel stays the default
+// and this one is the alternative route.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
