@@ -50,6 +50,8 @@ def _load():
             lib.oracle_round_bf16.restype = ctypes.c_float
             lib.oracle_pool_keys.argtypes = [i64, i32, i32, P, P]
             lib.oracle_pool_keys.restype = None
+            lib.oracle_pool_keys_gated.argtypes = [i64, i32, i32, P, P, P]
+            lib.oracle_pool_keys_gated.restype = None
             lib.oracle_indexer_scores.argtypes = [i64, i32, i32, P, P, P, P, i64, P]
             lib.oracle_indexer_scores.restype = None
             lib.oracle_topk.argtypes = [i64, i32, P, P, i64, P]
@@ -95,6 +97,17 @@ def pool_keys(k_I, round_to_bf16: bool) -> np.ndarray:
     assert L % 4 == 0
     out = np.empty((L // 4, di), np.float32)
     _load().oracle_pool_keys(L, di, int(bool(round_to_bf16)), _ptr(k_I), _ptr(out))
+    return out
+
+
+def pool_keys_gated(k_I, gate, round_to_bf16: bool) -> np.ndarray:
+    """kpool[p] = sum_j gate[4p+j] * k_I[4p+j] (fp32 fma chain in token order, then bf16 if asked)."""
+    k_I = _f32(k_I)
+    gate = _f32(gate)
+    L, di = k_I.shape
+    assert L % 4 == 0 and gate.shape == (L,)
+    out = np.empty((L // 4, di), np.float32)
+    _load().oracle_pool_keys_gated(L, di, int(bool(round_to_bf16)), _ptr(k_I), _ptr(gate), _ptr(out))
     return out
 
 

@@ -86,6 +86,27 @@ void oracle_pool_keys(int64_t L, int32_t di, int32_t round_to_bf16,
     }
 }
 
+/* Gated pool keys: the same pools, each token's key weighted by a per-token
+ * gate before the sum (page 1, "3. Context parallelism (CP)", names "k-pool
+ * gate scores" aligned with the keys and defines nothing more).  Reading:
+ * kpool[p] = sum_{j<4} gate[4p+j] * k_I[4p+j], accumulated in fp32 in token
+ * order with one fused multiply-add per token (acc = fma(g, k, acc) from
+ * acc = 0), then rounded once to the layer dtype.  With every gate 1 it is
+ * oracle_pool_keys exactly.  k_I: [L, di]; gate: [L]; kpool: [L/4, di]. */
+void oracle_pool_keys_gated(int64_t L, int32_t di, int32_t round_to_bf16,
+                            const float *k_I, const float *gate, float *kpool)
+{
+    int64_t P = L / 4;
+    for (int64_t p = 0; p < P; ++p) {
+        for (int32_t i = 0; i < di; ++i) {
+            float s = 0.0f;
+            for (int j = 0; j < 4; ++j)
+                s = fmaf(gate[4 * p + j], k_I[(4 * p + j) * di + i], s);
+            kpool[p * di + i] = round_to_bf16 ? oracle_round_bf16(s) : s;
+        }
+    }
+}
+
 /* Indexer scores for the listed query rows (page 1, "Model and bottleneck":
  * every query scores every pool; "1. DSA truly sparse": chunking by query
  * does not change what is computed).  q_I: [L, Hi, di]; kpool: [P, di];

@@ -62,6 +62,57 @@ def test_pool_keys_fp32_order_and_single_rounding():
     assert oracle.pool_keys(k_I, True)[0, 0] == np.float32(1 + 2 ** -7)
 
 
+def test_pool_keys_gated_unit_gates_are_the_plain_sum():
+    # fma(1, k, acc) rounds exactly like acc + k, so all-one gates give the plain pool bit for bit
+    rng = np.random.default_rng(21)
+    k_I = rng.standard_normal((256, 32)).astype(np.float32)
+    g = np.ones(256, np.float32)
+    for rnd in (False, True):
+        assert np.array_equal(oracle.pool_keys_gated(k_I, g, rnd).view(np.uint32),
+                              oracle.pool_keys(k_I, rnd).view(np.uint32))
+
+
+def test_pool_keys_gated_one_hot_gates_pick_one_token():
+    rng = np.random.default_rng(22)
+    L, di = 64, 16
+    k_I = rng.standard_normal((L, di)).astype(np.float32)
+    pick = rng.integers(0, 4, size=L // 4)
+    g = np.zeros(L, np.float32)
+    g[4 * np.arange(L // 4) + pick] = 1.0
+    expect = k_I[4 * np.arange(L // 4) + pick]
+    assert np.array_equal(oracle.pool_keys_gated(k_I, g, False), expect)
+    assert np.array_equal(oracle.pool_keys_gated(k_I, np.zeros(L, np.float32), False), np.zeros((L // 4, di)))
+
+
+def test_pool_keys_gated_integer_inputs_equal_weighted_block_sum():
+    # small integers: every product and partial sum is exact in fp32, so the result is the
+    # exact weighted sum, computed here in int64 by numpy
+    rng = np.random.default_rng(23)
+    L, di = 128, 8
+    k_I = rng.integers(-3, 4, size=(L, di))
+    g = rng.integers(-2, 5, size=L)
+    expect = (g[:, None] * k_I).reshape(L // 4, 4, di).sum(axis=1)
+    for rnd in (False, True):   # |sum| <= 48: exact in bf16 as well
+        assert np.array_equal(oracle.pool_keys_gated(k_I.astype(np.float32), g.astype(np.float32), rnd), expect)
+
+
+def test_pool_keys_gated_fma_chain_and_single_rounding():
+    # one token: gate 1 + 2^-12 times key 1 + 2^-12 = 1 + 2^-11 + 2^-24 exactly; the first fma
+    # from 0 rounds it to fp32 (a tie, to even: 1 + 2^-11), then fma with the next token
+    # 2^-24 * 1 lands on the tie again (1 + 2^-11 + 2^-24 -> 1 + 2^-11)
+    a = np.float32(1 + 2.0 ** -12)
+    k_I = np.array([[a], [1.0], [0.0], [0.0]], np.float32)
+    g = np.array([a, 2.0 ** -24, 0.0, 0.0], np.float32)
+    assert oracle.pool_keys_gated(k_I, g, False)[0, 0] == np.float32(1 + 2.0 ** -11)
+    # fused, not multiply-then-add: token 0 leaves acc = -(3 + 2^-21); token 1's product
+    # 3 * (1 + 2^-23) = 3 + 3*2^-23 is not exact in fp32.  One fma gives the exact
+    # -(3 + 2^-21) + 3 + 3*2^-23 = -2^-23; rounding the product first (a tie, to even:
+    # 3 + 2^-21) and then adding would give 0.
+    k_I = np.array([[-(3 + 2.0 ** -21)], [1 + 2.0 ** -23], [0.0], [0.0]], np.float32)
+    g = np.array([1.0, 3.0, 0.0, 0.0], np.float32)
+    assert oracle.pool_keys_gated(k_I, g, False)[0, 0] == np.float32(-(2.0 ** -23))
+
+
 # ------------------------------------------------------------------ indexer
 def _rand_idx_inputs(rng, L, Hi, di, positive=False):
     if positive:
