@@ -140,6 +140,24 @@ size_t dsa_bwd_workspace_bytes(const dsa_dims *dims);
  * Bitwise equal to the definition (fp32 sum in token order, one rounding). */
 dsa_status dsa_pool_keys(const dsa_dims *dims, const void *k_idx, void *kpool, dsa_stream_t stream);
 
+/* Gated pool keys: each token's key weighted by a per-token gate before the
+ * pool's sum.  Same page, section "3. Context parallelism (CP)", names k-pool
+ * gate scores that must stay aligned with the keys and defines nothing more;
+ * the reading implemented is
+ *   kpool[p] = sum_{j<4} gate[4p+j] * k_idx[4p+j]
+ * accumulated in fp32 in token order with one fused multiply-add per token
+ * (from 0), then rounded once to the layer dtype.  With every gate 1 it is
+ * dsa_pool_keys bit for bit.  Any normalisation of the gates (a softmax over
+ * the pool, say) is the caller's; the result feeds dsa_indexer_score or
+ * dsa_indexer_topk exactly as dsa_pool_keys' does.
+ *   k_idx  [L, di]   layer dtype
+ *   gate   [L]       fp32, 16-byte aligned
+ *   kpool  [L/4, di] layer dtype, output
+ * Bitwise equal to that definition.  Returns DSA_ERR_INVALID_ARG for a NULL
+ * or misaligned pointer, before any launch. */
+dsa_status dsa_pool_keys_gated(const dsa_dims *dims, const void *k_idx, const float *gate, void *kpool,
+                               dsa_stream_t stream);
+
 /* Indexer scores for queries q_begin .. q_begin+q_count-1.  Same page,
  * sections "Model and bottleneck" and "1. DSA truly sparse" (chunked by
  * query).  bf16 runs on the tcgen05 tensor cores (fp32 accumulation in

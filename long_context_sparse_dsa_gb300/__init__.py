@@ -67,6 +67,7 @@ def _load():
             "dsa_workspace_bytes": ([D], ctypes.c_size_t),
             "dsa_bwd_workspace_bytes": ([D], ctypes.c_size_t),
             "dsa_pool_keys": ([D, P, P, P], ctypes.c_int),
+            "dsa_pool_keys_gated": ([D, P, P, P, P], ctypes.c_int),
             "dsa_indexer_score": ([D, P, P, P, i64, i64, P, P], ctypes.c_int),
             "dsa_topk": ([D, P, i64, i64, P, P], ctypes.c_int),
             "dsa_indexer_topk": ([D, P, P, P, i64, i64, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -152,6 +153,12 @@ def bwd_workspace_bytes(dims: Dims) -> int:
 
 def pool_keys(dims, k_idx, kpool, stream=None):
     _check(_load().dsa_pool_keys(ctypes.byref(dims), _ptr(k_idx), _ptr(kpool), _stream(stream)), "dsa_pool_keys")
+
+
+def pool_keys_gated(dims, k_idx, gate, kpool, stream=None):
+    """kpool[p] = sum_j gate[4p+j] * k_idx[4p+j] (gate: [L] fp32)."""
+    _check(_load().dsa_pool_keys_gated(ctypes.byref(dims), _ptr(k_idx), _ptr(gate), _ptr(kpool), _stream(stream)),
+           "dsa_pool_keys_gated")
 
 
 def indexer_score(dims, q_idx, kpool, w, q_begin, q_count, scores, stream=None):

@@ -98,8 +98,8 @@ dsa_status check_range(const dsa_dims* d, int64_t q_begin, int64_t q_count) {
 
 bool is_bf16(const dsa_dims* d) { return d->dtype == DSA_BF16; }
 
-dsa_status do_pool(const dsa_dims* d, const void* k_idx, void* kpool, cudaStream_t s) {
-  return cuda_status(dsa::launch_pool_keys(is_bf16(d), d->L, d->di, k_idx, kpool, s), "pool_keys launch");
+dsa_status do_pool(const dsa_dims* d, const void* k_idx, void* kpool, cudaStream_t s, const float* gate = nullptr) {
+  return cuda_status(dsa::launch_pool_keys(is_bf16(d), d->L, d->di, k_idx, gate, kpool, s), "pool_keys launch");
 }
 
 dsa_status do_score(const dsa_dims* d, const void* q_idx, const void* kpool, const float* w, int64_t q_begin,
@@ -262,6 +262,17 @@ dsa_status dsa_pool_keys(const dsa_dims* dims, const void* k_idx, void* kpool, d
   REQUIRE_PTR(k_idx);
   REQUIRE_PTR(kpool);
   return do_pool(dims, k_idx, kpool, (cudaStream_t)stream);
+}
+
+dsa_status dsa_pool_keys_gated(const dsa_dims* dims, const void* k_idx, const float* gate, void* kpool,
+                               dsa_stream_t stream) {
+  g_msg[0] = 0;
+  dsa_status st = check_dims(dims, false);
+  if (st) return st;
+  REQUIRE_PTR(k_idx);
+  REQUIRE_PTR(gate);
+  REQUIRE_PTR(kpool);
+  return do_pool(dims, k_idx, kpool, (cudaStream_t)stream, gate);
 }
 
 dsa_status dsa_indexer_score(const dsa_dims* dims, const void* q_idx, const void* kpool, const float* w,

@@ -9,7 +9,9 @@
 namespace dsa {
 
 // Pool keys: kpool[p] = sum of k_I rows 4p..4p+3 (fp32 adds in order, one rounding).
-cudaError_t launch_pool_keys(bool bf16, int64_t L, int di, const void* k_idx, void* kpool, cudaStream_t s);
+// gate: [L] fp32 per-token gates, or nullptr for the plain sum
+cudaError_t launch_pool_keys(bool bf16, int64_t L, int di, const void* k_idx, const float* gate, void* kpool,
+                             cudaStream_t s);
 
 // Indexer scores, fp32 layer: plain FFMA kernel.
 cudaError_t launch_indexer_simt_f32(int64_t L, int Hi, int di, const float* q_idx, const float* kpool,

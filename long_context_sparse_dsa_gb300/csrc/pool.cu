@@ -6,6 +6,13 @@
 // HBM-bound and tiny: each thread moves 16 bytes of one pool row (8 bf16 or 4
 // fp32 values) from each of the pool's 4 token rows, so every load and store
 // is a coalesced 16-byte access.
+//
+// Gated variant (same page, section "3. Context parallelism (CP)", which names
+// k-pool gate scores aligned with the keys and defines nothing more): each
+// token's key is weighted by a per-token fp32 gate before the sum,
+// kpool[p,:] = sum_j gate[4p+j] * k_I[4p+j,:], as one fused multiply-add per
+// token from zero in token order, rounded once.  All-one gates give the plain
+// pool bit for bit.
 #include "common.cuh"
 #include "launch.h"
 
@@ -51,9 +58,9 @@ __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* f) {
   return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
 }
 
-template <typename T>
-__global__ void pool_keys_kernel(const uint4* __restrict__ k_idx, uint4* __restrict__ kpool, int64_t P,
-                                 int vec_per_row) {
+template <typename T, bool GATED>
+__global__ void pool_keys_kernel(const uint4* __restrict__ k_idx, const float* __restrict__ gate,
+                                 uint4* __restrict__ kpool, int64_t P, int vec_per_row) {
   constexpr int N = Vec16<T>::N;
   const int64_t total = P * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -61,18 +68,32 @@ __global__ void pool_keys_kernel(const uint4* __restrict__ k_idx, uint4* __restr
     const int c = (int)(i - p * vec_per_row);
     const uint4* src = k_idx + (4 * p) * vec_per_row + c;
     float acc[N], x[N];
-    unpack16<T>(__ldg(src), acc);
+    if constexpr (GATED) {
+      const float4 g = __ldg(reinterpret_cast<const float4*>(gate) + p);   // the pool's 4 gates
+      const float gj[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int j = 1; j < 4; ++j) {
-      unpack16<T>(__ldg(src + j * vec_per_row), x);
+      for (int e = 0; e < N; ++e) acc[e] = 0.f;
 #pragma unroll
-      for (int e = 0; e < N; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+      for (int j = 0; j < 4; ++j) {
+        unpack16<T>(__ldg(src + j * vec_per_row), x);
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[e] = __fmaf_rn(gj[j], x[e], acc[e]);
+      }
+    } else {
+      unpack16<T>(__ldg(src), acc);
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        unpack16<T>(__ldg(src + j * vec_per_row), x);
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+      }
     }
     kpool[i] = pack16<T>(acc);
   }
 }
 
-cudaError_t launch_pool_keys(bool bf16, int64_t L, int di, const void* k_idx, void* kpool, cudaStream_t s) {
+cudaError_t launch_pool_keys(bool bf16, int64_t L, int di, const void* k_idx, const float* gate, void* kpool,
+                             cudaStream_t s) {
   const int64_t P = L / 4;
   const int vec = bf16 ? di / 8 : di / 4;
   const int64_t total = P * vec;
@@ -81,12 +102,19 @@ cudaError_t launch_pool_keys(bool bf16, int64_t L, int di, const void* k_idx, vo
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (bf16)
-    pool_keys_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, s>>>(
-        static_cast<const uint4*>(k_idx), static_cast<uint4*>(kpool), P, vec);
-  else
-    pool_keys_kernel<float><<<(unsigned)blocks, threads, 0, s>>>(static_cast<const uint4*>(k_idx),
-                                                                  static_cast<uint4*>(kpool), P, vec);
+  auto src = static_cast<const uint4*>(k_idx);
+  auto dst = static_cast<uint4*>(kpool);
+  if (bf16) {
+    if (gate)
+      pool_keys_kernel<__nv_bfloat16, true><<<(unsigned)blocks, threads, 0, s>>>(src, gate, dst, P, vec);
+    else
+      pool_keys_kernel<__nv_bfloat16, false><<<(unsigned)blocks, threads, 0, s>>>(src, nullptr, dst, P, vec);
+  } else {
+    if (gate)
+      pool_keys_kernel<float, true><<<(unsigned)blocks, threads, 0, s>>>(src, gate, dst, P, vec);
+    else
+      pool_keys_kernel<float, false><<<(unsigned)blocks, threads, 0, s>>>(src, nullptr, dst, P, vec);
+  }
   return cudaGetLastError();
 }
 

@@ -192,3 +192,13 @@ def test_route_setters_accept_only_their_routes(lib):
         assert setter(2) == 1 and setter(-1) == 1          # DSA_ERR_INVALID_ARG
         assert setter(0) == 0 and setter(1) == 0
         assert setter(default) == 0
+
+
+def test_gated_pool_keys_validates_before_launch(lib):
+    """NULL or misaligned pointers are rejected before anything is enqueued
+    (the pointers below are never dereferenced: validation fails first)."""
+    dims = dsa.make_dims(1024, 16, 128, 8, 64, 64)
+    good = ctypes.c_void_p(1 << 20)
+    for k, g, out in ((None, good, good), (good, None, good), (good, good, None),
+                      (good, ctypes.c_void_p((1 << 20) + 4), good)):
+        assert lib.dsa_pool_keys_gated(ctypes.byref(dims), k, g, out, None) == 1   # DSA_ERR_INVALID_ARG

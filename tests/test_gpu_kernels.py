@@ -101,6 +101,55 @@ def test_pool_keys_bitexact(dtype, di):
     assert np.array_equal(_f32(kp).view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("dtype,di", [("bf16", 64), ("bf16", 128), ("fp32", 64), ("fp32", 128)])
+def test_pool_keys_gated_bitexact(dtype, di):
+    """Gated pooling against the oracle bit for bit (N(0,1)-scale keys, gates
+    of both signs and assorted magnitudes), and all-one gates against the plain
+    pool."""
+    g = torch.Generator().manual_seed(31)
+    L = 4 * 1331
+    k_I = (torch.randn(L, di, generator=g) * 3).to(_tdt(dtype))
+    gate = torch.randn(L, generator=g) * torch.exp2(torch.randint(-6, 7, (L,), generator=g).float())
+    dims = dsa.make_dims(L, 16 if dtype == "bf16" else 8, 128, 8, di, 8, dtype=dtype)
+    kp = torch.empty((L // 4, di), dtype=_tdt(dtype), device=DEV)
+    dsa.pool_keys_gated(dims, k_I.to(DEV), gate.to(DEV), kp)
+    ref = oracle.pool_keys_gated(_f32(k_I), gate.numpy(), dtype == "bf16")
+    assert np.array_equal(_f32(kp).view(np.uint32), ref.view(np.uint32))
+    ones = torch.ones(L, device=DEV)
+    kp1, kp0 = torch.empty_like(kp), torch.empty_like(kp)
+    dsa.pool_keys_gated(dims, k_I.to(DEV), ones, kp1)
+    dsa.pool_keys(dims, k_I.to(DEV), kp0)
+    dsa.check_device_error()
+    assert torch.equal(kp1.view(torch.uint8), kp0.view(torch.uint8))
+
+
+def test_gated_pools_feed_the_selection_bitexact():
+    """The gated pool keys through the indexer and top-k (dsa_indexer_topk, both
+    routes): with integer keys and gates every score is an exact integer, so the
+    selection equals the oracle's bit for bit."""
+    g = torch.Generator().manual_seed(32)
+    L, Hi, di, k = 4096, 8, 64, 64
+    q_I, k_I, w = _int_inputs(g, L, Hi, di, "bf16")
+    gate = torch.randint(-1, 3, (L,), generator=g).float()
+    dims = dsa.make_dims(L, 16, 128, Hi, di, k, q_chunk=1500, dtype="bf16")
+    kp = torch.empty((L // 4, di), dtype=torch.bfloat16, device=DEV)
+    dsa.pool_keys_gated(dims, k_I.to(DEV), gate.to(DEV), kp)
+    kp_ref = oracle.pool_keys_gated(_f32(k_I), gate.numpy(), True)
+    assert np.array_equal(_f32(kp).view(np.uint32), kp_ref.view(np.uint32))
+    idx_ref = oracle.topk(oracle.indexer_scores(_f32(q_I), kp_ref, _f32(w)), L, k)
+    ws = torch.empty(dsa.workspace_bytes(dims), dtype=torch.uint8, device=DEV)
+    try:
+        for route in (1, 0):
+            dsa.set_indexer_topk_route(route)
+            idx = torch.full((L, k), -7, dtype=torch.int32, device=DEV)
+            for q0 in range(0, L, 1500):
+                dsa.indexer_topk(dims, q_I.to(DEV), kp, w.to(DEV), q0, min(1500, L - q0), idx, ws)
+            dsa.check_device_error()
+            assert np.array_equal(idx.cpu().numpy(), idx_ref), route
+    finally:
+        dsa.set_indexer_topk_route(1)
+
+
 # ---------------------------------------------------------------- indexer
 @pytest.mark.parametrize("dtype,Hi,di", [("bf16", 8, 64), ("bf16", 8, 128), ("bf16", 4, 64), ("bf16", 4, 128),
                                          ("fp32", 4, 64), ("fp32", 3, 128)])
