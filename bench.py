@@ -484,7 +484,9 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
     return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3), "mode": mode,
-            "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev)}
+            "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev),
+            # the runtime's hardware work queues per device (unset: the runtime's default)
+            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS")}
 
 
 def copy_bandwidth(host, names, d_in, outs, stream, dev):

@@ -76,7 +76,8 @@ class _Lib:
 
 
 @pytest.mark.parametrize("with_bwd", [True, False])
-def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd):
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd, steps):
     rec = _Rec()
     _install(monkeypatch, rec)
     names = ["Q", "K", "V", "q_I", "k_I", "w"] + (["dO"] if with_bwd else [])
@@ -84,7 +85,6 @@ def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd):
     d_in = {n: torch.zeros(4, 3) for n in names}
     bufs = types.SimpleNamespace(o=torch.zeros(4, 3), lse=torch.zeros(4), idx=None, kpool=None, ws=None, o_acc=None)
     grads = (torch.zeros(4, 3), torch.zeros(4), torch.zeros(4)) if with_bwd else (None, None, None)
-    steps = 5
     # the copy-rate measurement after the pipelined run is not part of the schedule
     monkeypatch.setattr(bench, "copy_bandwidth", lambda *a, **kw: {})
     r = bench.end_to_end(_Lib(rec), None, types.SimpleNamespace(L=1000), host, d_in, bufs, *grads, None,
@@ -94,36 +94,42 @@ def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd):
     assert r["h2d_bytes_per_step"] == sum(t.numel() * t.element_size() for t in host.values())
     assert all(torch.equal(d_in[n], host[n]) for n in names)
 
-    # reconstruct per step: the event ids recorded after the input copy, the
-    # layer and the output copy, and the waits issued before each of them
-    records = [op for op in rec.ops if op[0] == "record"]
-    start, per_step = records[0], records[1:]
-    assert len(per_step) == 3 * steps
-    in_done = [per_step[3 * i][2] for i in range(steps)]
-    run_done = [per_step[3 * i + 1][2] for i in range(steps)]
-    out_done = [per_step[3 * i + 2][2] for i in range(steps)]
-    streams = {per_step[3 * i + j][1] for i in range(steps) for j in range(3)}
-    assert len(streams) == 3 and start[1] == per_step[0][1]
+    # The three streams, identified by what is issued on them: input copies are
+    # recorded on one stream (plus the start event), layers on another, output
+    # copies on the third; on each stream the events come in step order.
     layers = [op for op in rec.ops if op[0] == "fwd"]
     assert len(layers) == steps
-    # the two buffer sets alternate
-    assert layers[0][2] != layers[1][2] and layers[0][2] == layers[2][2]
+    run_stream = layers[0][1]
+    records = [op for op in rec.ops if op[0] == "record"]
+    start = records[0]
+    by_stream = {}
+    for op in records[1:]:
+        by_stream.setdefault(op[1], []).append(op)
+    assert run_stream in by_stream and len(by_stream) == 3
+    in_stream = start[1]
+    out_stream = next(st for st in by_stream if st not in (in_stream, run_stream))
+    in_done = [op[2] for op in by_stream[in_stream]]
+    run_done = [op[2] for op in by_stream[run_stream]]
+    out_done = [op[2] for op in by_stream[out_stream]]
+    assert len(in_done) == len(run_done) == len(out_done) == steps
+    if steps >= 3:
+        # the two buffer sets alternate
+        assert layers[0][2] != layers[1][2] and layers[0][2] == layers[2][2]
 
-    def waits_before(kind_index):
-        """Waits issued between the previous record and this step's record."""
-        pos = rec.ops.index(kind_index)
+    def waits_before(event_id):
+        """Waits issued on the event's stream between its previous record and this one."""
+        pos = next(i for i, op in enumerate(rec.ops) if op[0] == "record" and op[2] == event_id)
+        stream = rec.ops[pos][1]
         out = []
         for op in reversed(rec.ops[:pos]):
-            if op[0] == "record":
+            if op[0] == "record" and op[1] == stream:
                 break
-            if op[0] == "wait":
+            if op[0] == "wait" and op[1] == stream:
                 out.append(op[2])
         return set(out)
 
     for i in range(steps):
-        w_in = waits_before(per_step[3 * i])
-        w_run = waits_before(per_step[3 * i + 1])
-        w_out = waits_before(per_step[3 * i + 2])
+        w_in, w_run, w_out = waits_before(in_done[i]), waits_before(run_done[i]), waits_before(out_done[i])
         assert in_done[i] in w_run                       # the layer waits for its inputs
         assert run_done[i] in w_out                      # the copy-out waits for the layer
         if i >= 2:
