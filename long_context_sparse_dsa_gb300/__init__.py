@@ -176,7 +176,8 @@ def indexer_topk_workspace_bytes(dims, q_count) -> int:
 
 
 def indexer_topk(dims, q_idx, kpool, w, q_begin, q_count, idx, ws, ws_bytes=None, stream=None):
-    """Fused indexer + top-k of one query range (no score block for bf16 layers)."""
+    """Indexer + top-k of one query range in one call; for bf16 layers route 1 (default) uses the score
+    block in ws, route 0 the candidate lists (set_indexer_topk_route)."""
     if ws_bytes is None:
         ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(_load().dsa_indexer_topk(ctypes.byref(dims), _ptr(q_idx), _ptr(kpool), _ptr(w), int(q_begin), int(q_count),
