@@ -67,8 +67,8 @@ TRAFFIC = {
     # mean over the 16 chunk launches of one step
     ("bf16_128k_needle", "indexer"): {"bytes": 37685632 + 480333056,
                                       "sources": {"indexer_tc.cu": "6267c910c1505ced", "common.cuh": "4c65dfd5da7caf78"}},
-    ("bf16_128k_needle", "topk"): {"bytes": 538221632 + 11386624,
-                                   "sources": {"topk.cu": "3a87db186862256b", "common.cuh": "4c65dfd5da7caf78"}},
+    ("bf16_128k_needle", "topk"): {"bytes": 538500512 + 11403616,
+                                   "sources": {"topk.cu": "7e34eb4699bcd34b", "common.cuh": "4c65dfd5da7caf78"}},
 }
 
 
