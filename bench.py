@@ -474,8 +474,9 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
             dsa.layer_bwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o, lse, d["dO"], grads[0], grads[1], grads[2],
                           bws, stream=s, o_acc=bufs.o_acc)
 
+    overlap = None
     try:
-        ms = _e2e_pipelined(host, names, d_in, outs, layer, steps, dev)
+        ms, overlap = _e2e_pipelined(host, names, d_in, outs, layer, steps, dev)
         mode = "pipelined: 3 streams, 2 device buffer sets"
     except Exception as exc:   # reported in the JSON line, never silent
         torch.cuda.synchronize(dev)
@@ -484,6 +485,7 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
     return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3), "mode": mode,
+            "overlap": overlap,
             "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev),
             # the runtime's hardware work queues per device (unset: the runtime's default)
             "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS")}
@@ -549,7 +551,25 @@ def _e2e_pipelined(host, names, d_in, outs, layer, steps, dev):
                 dst.copy_(src, non_blocking=True)
         out_done[i].record(s_out)
     torch.cuda.synchronize(dev)
-    return start.elapsed_time(out_done[-1])
+    # Where the time went, from the same events: layer i can begin once its
+    # inputs are in, its buffer set's previous outputs are out and layer i-1 is
+    # done; from then to its end is its time inside the pipeline, and the run
+    # stream's wait before it is copy time the pipeline did not hide.
+    t = start.elapsed_time
+    layer_ms, wait_ms = [], []
+    for i in range(steps):
+        begin = t(in_done[i])
+        if i >= 1:
+            begin = max(begin, t(run_done[i - 1]))
+        if i >= 2:
+            begin = max(begin, t(out_done[i - 2]))
+        layer_ms.append(t(run_done[i]) - begin)
+        if i >= 1:
+            wait_ms.append(begin - t(run_done[i - 1]))
+    overlap = {"layer_ms_mean": round(sum(layer_ms) / steps, 3), "layer_ms_max": round(max(layer_ms), 3),
+               "run_stream_wait_ms_mean": round(sum(wait_ms) / len(wait_ms), 3) if wait_ms else None,
+               "fill_ms": round(t(in_done[0]), 3), "drain_ms": round(t(out_done[-1]) - t(run_done[-1]), 3)}
+    return t(out_done[-1]), overlap
 
 
 def _e2e_serial(host, names, d_in, outs, layer, steps, stream, dev):

@@ -91,6 +91,12 @@ def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd, ste
                          torch.cuda.Stream(), types.SimpleNamespace(steps=steps, e2e_steps=steps), with_bwd, 1, "cpu")
     assert r["mode"].startswith("pipelined")
     assert r["steps"] == steps
+    ov = r["overlap"]
+    assert set(ov) == {"layer_ms_mean", "layer_ms_max", "run_stream_wait_ms_mean", "fill_ms", "drain_ms"}
+    assert ov["layer_ms_max"] >= ov["layer_ms_mean"] > 0
+    assert (ov["run_stream_wait_ms_mean"] is None) == (steps == 1)
+    if steps > 1:
+        assert ov["run_stream_wait_ms_mean"] >= 0
     assert r["h2d_bytes_per_step"] == sum(t.numel() * t.element_size() for t in host.values())
     assert all(torch.equal(d_in[n], host[n]) for n in names)
 
