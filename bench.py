@@ -452,35 +452,52 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     copies its inputs in from pinned host memory, runs the layer and copies its
     outputs (O, LSE and, with a backward, dQ, dK, dV) back to pinned memory.
 
-    Consecutive steps are pipelined over three streams with two device buffer
-    sets: the inputs of step i+1 go in and the outputs of step i-1 come back
-    while step i runs, and each step's copies still precede and follow its own
-    layer.  --e2e-steps steps (10 by default) are timed, pipeline fill and drain included, and
-    the box's measured copy rates are reported beside the figure.  If the
-    pipelined run raises, the serialised run is reported and "mode" says why."""
+    The layer runs as its three phases, each through its own entry points:
+    pool keys and indexer + top-k per query chunk (what dsa_layer_fwd does
+    first), the attention forward, the backward.  Consecutive steps are
+    pipelined over three streams with two device buffer sets: a phase waits
+    only for its own inputs (k_I, q_I, w; then Q, K, V; then dO), and O and
+    LSE go back as soon as the forward is done, so the copies of one step
+    overlap the phases of its neighbours and of itself.  --e2e-steps steps (10
+    by default) are timed, pipeline fill and drain included, and the box's
+    measured copy rates are reported beside the figure.  If the pipelined run
+    raises, the serialised run is reported and "mode" says why."""
     names = list(d_in.keys())
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
     d2h = sum(t.numel() * t.element_size() for t in outs)
     steps = max(1, args.e2e_steps)
+    C = int(dims.q_chunk)
+    chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
 
-    def layer(d, o, lse, grads, s):
-        dsa.layer_fwd(dims, d["Q"], d["K"], d["V"], d["q_I"], d["k_I"], d["w"], o, lse, bufs.idx, bufs.kpool,
-                      bufs.ws, stream=s, o_acc=bufs.o_acc)
+    def select(d, o, s):       # writes kpool, idx (and the indexer workspace)
+        dsa.pool_keys(dims, d["k_I"], bufs.kpool, s)
+        for q0, n in chunks:
+            dsa.indexer_topk(dims, d["q_I"], bufs.kpool, d["w"], q0, n, bufs.idx, bufs.ws, stream=s)
+
+    def forward(d, o, s):      # writes O, LSE, o_acc
+        dsa.sparse_attn_fwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o[0], o[1], s, o_acc=bufs.o_acc)
+
+    def backward(d, o, s):     # writes dQ, dK, dV
         if det:
-            dsa.sparse_attn_bwd_det(dims, d["Q"], d["K"], d["V"], bufs.idx, o, lse, d["dO"], grads[0], grads[1],
-                                    grads[2], bws, stream=s, o_acc=bufs.o_acc)
-        elif with_bwd:
-            dsa.layer_bwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o, lse, d["dO"], grads[0], grads[1], grads[2],
-                          bws, stream=s, o_acc=bufs.o_acc)
+            dsa.sparse_attn_bwd_det(dims, d["Q"], d["K"], d["V"], bufs.idx, o[0], o[1], d["dO"], o[2], o[3], o[4],
+                                    bws, stream=s, o_acc=bufs.o_acc)
+        else:
+            dsa.layer_bwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o[0], o[1], d["dO"], o[2], o[3], o[4], bws,
+                          stream=s, o_acc=bufs.o_acc)
 
+    # (inputs the phase needs, the phase, indices into outs it completes)
+    phases = [(["k_I", "q_I", "w"], select, []), (["Q", "K", "V"], forward, [0, 1])]
+    if with_bwd:
+        phases.append((["dO"], backward, [2, 3, 4]))
+    assert sorted(n for ph in phases for n in ph[0]) == sorted(names)
     overlap = None
     try:
-        ms, overlap = _e2e_pipelined(host, names, d_in, outs, layer, steps, dev)
-        mode = "pipelined: 3 streams, 2 device buffer sets"
+        ms, overlap = _e2e_pipelined(host, d_in, outs, phases, steps, dev)
+        mode = "pipelined: 3 streams, 2 device buffer sets, per-phase copies"
     except Exception as exc:   # reported in the JSON line, never silent
         torch.cuda.synchronize(dev)
-        ms = _e2e_serial(host, names, d_in, outs, layer, steps, stream, dev)
+        ms = _e2e_serial(host, names, d_in, outs, phases, steps, stream, dev)
         mode = f"serialised on one stream (pipelined run raised {type(exc).__name__}: {exc})"[:240]
     value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
     return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -519,69 +536,85 @@ def copy_bandwidth(host, names, d_in, outs, stream, dev):
             "d2h_gbs": round(d2h_b / (ms_out * 1e-3) / 1e9, 1), "d2h_ms": round(ms_out, 3)}
 
 
-def _e2e_pipelined(host, names, d_in, outs, layer, steps, dev):
-    """Total ms of `steps` pipelined steps (see end_to_end)."""
+def _e2e_pipelined(host, d_in, outs, phases, steps, dev):
+    """Total ms of `steps` pipelined steps (see end_to_end) and where it went."""
+    names = [n for ph in phases for n in ph[0]]
     sets = [(d_in, outs), ({n: torch.empty_like(d_in[n]) for n in names}, [torch.empty_like(t) for t in outs])]
     pinned = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in sets]
     s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    P = len(phases)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
-    in_done, run_done, out_done = [ev() for _ in range(steps)], [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+    in_done = [[ev() for _ in range(P)] for _ in range(steps)]     # a phase's inputs are in
+    ph_done = [[ev() for _ in range(P)] for _ in range(steps)]     # a phase has run
+    out_done = [[ev() for _ in range(P)] for _ in range(steps)]    # a phase's outputs are out
     torch.cuda.synchronize(dev)
     start = ev()
     start.record(s_in)
     for i in range(steps):
         d, o = sets[i % 2]
         if i >= 2:
-            s_in.wait_event(run_done[i - 2])      # step i-2 has finished reading this input set
-        with torch.cuda.stream(s_in):
-            for n in names:
-                d[n].copy_(host[n], non_blocking=True)
-        in_done[i].record(s_in)
-        s_run.wait_event(in_done[i])
-        if i >= 2:
-            s_run.wait_event(out_done[i - 2])     # step i-2's outputs in this set have been copied out
-        layer(d, o[0], o[1], o[2:], s_run)
-        run_done[i].record(s_run)
-        s_out.wait_event(run_done[i])
-        with torch.cuda.stream(s_out):
-            for src, dst in zip(o, pinned[i % 2]):
-                dst.copy_(src, non_blocking=True)
-        out_done[i].record(s_out)
+            s_in.wait_event(ph_done[i - 2][-1])   # step i-2 has finished reading this input set
+        for p, (inputs, _, _) in enumerate(phases):
+            with torch.cuda.stream(s_in):
+                for n in inputs:
+                    d[n].copy_(host[n], non_blocking=True)
+            in_done[i][p].record(s_in)
+        for p, (_, run, outputs) in enumerate(phases):
+            s_run.wait_event(in_done[i][p])
+            if i >= 2 and outputs:
+                s_run.wait_event(out_done[i - 2][p])   # step i-2's outputs in this set have been copied out
+            run(d, o, s_run)
+            ph_done[i][p].record(s_run)
+            if outputs:
+                s_out.wait_event(ph_done[i][p])
+                with torch.cuda.stream(s_out):
+                    for j in outputs:
+                        pinned[i % 2][j].copy_(o[j], non_blocking=True)
+                out_done[i][p].record(s_out)
     torch.cuda.synchronize(dev)
-    # Where the time went, from the same events: layer i can begin once its
-    # inputs are in, its buffer set's previous outputs are out and layer i-1 is
-    # done; from then to its end is its time inside the pipeline, and the run
-    # stream's wait before it is copy time the pipeline did not hide.
+    # Where the time went, from the same events: a phase can begin once its
+    # inputs are in, its buffer set's previous outputs are out and the phase
+    # before it is done; from then to its end is its time inside the pipeline,
+    # and the run stream's wait before it is copy time the pipeline did not hide.
     t = start.elapsed_time
+    last_out = max(p for p in range(P) if phases[p][2])
     layer_ms, wait_ms = [], []
     for i in range(steps):
-        begin = t(in_done[i])
-        if i >= 1:
-            begin = max(begin, t(run_done[i - 1]))
-        if i >= 2:
-            begin = max(begin, t(out_done[i - 2]))
-        layer_ms.append(t(run_done[i]) - begin)
-        if i >= 1:
-            wait_ms.append(begin - t(run_done[i - 1]))
+        run_ms = waited = 0.0
+        for p, (_, _, outputs) in enumerate(phases):
+            ready = t(in_done[i][p])
+            if i >= 2 and outputs:
+                ready = max(ready, t(out_done[i - 2][p]))
+            anchor = t(ph_done[i][p - 1]) if p > 0 else (t(ph_done[i - 1][-1]) if i > 0 else None)
+            begin = ready if anchor is None else max(ready, anchor)
+            if anchor is not None:
+                waited += begin - anchor
+            run_ms += t(ph_done[i][p]) - begin
+        layer_ms.append(run_ms)
+        wait_ms.append(waited)
     overlap = {"layer_ms_mean": round(sum(layer_ms) / steps, 3), "layer_ms_max": round(max(layer_ms), 3),
-               "run_stream_wait_ms_mean": round(sum(wait_ms) / len(wait_ms), 3) if wait_ms else None,
-               "fill_ms": round(t(in_done[0]), 3), "drain_ms": round(t(out_done[-1]) - t(run_done[-1]), 3)}
-    return t(out_done[-1]), overlap
+               "run_stream_wait_ms_mean": round(sum(wait_ms) / steps, 3),
+               "fill_ms": round(t(in_done[0][0]), 3),
+               "drain_ms": round(t(out_done[-1][last_out]) - t(ph_done[-1][-1]), 3)}
+    return t(out_done[-1][last_out]), overlap
 
 
-def _e2e_serial(host, names, d_in, outs, layer, steps, stream, dev):
+def _e2e_serial(host, names, d_in, outs, phases, steps, stream, dev):
     """Total ms of `steps` steps with every copy and launch on one stream."""
     pinned = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
 
     def one():
-        for n in names:
-            d_in[n].copy_(host[n], non_blocking=True)
-        layer(d_in, outs[0], outs[1], outs[2:], stream)
-        for src, dst in zip(outs, pinned):
-            dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(stream):
+            for n in names:
+                d_in[n].copy_(host[n], non_blocking=True)
+        for _, run, _ in phases:
+            run(d_in, outs, stream)
+        with torch.cuda.stream(stream):
+            for src, dst in zip(outs, pinned):
+                dst.copy_(src, non_blocking=True)
 
     one()
     torch.cuda.synchronize(dev)

@@ -1,7 +1,14 @@
 """The end-to-end timing schedule of bench.py, on CPU with stand-ins for CUDA
-streams and events: two device buffer sets over three streams.  Every step's
-input copy, layer and output copy must be ordered so that no buffer set is
-overwritten while an earlier step still uses it."""
+streams and events.
+
+The pipelined schedule runs each step's three phases (indexer + top-k, the
+forward, the backward) on one stream, the input copies on a second and the
+output copies on a third, over two device buffer sets.  The stand-ins record
+every copy and every library call with the buffers it reads and writes, and
+vector clocks give the happens-before order that stream order and event
+waits establish.  The check: every two accesses to one buffer, at least one
+of them a write, are ordered -- no buffer is overwritten while an earlier
+step still reads it, and nothing is read before it is written."""
 import types
 
 import pytest
@@ -11,23 +18,47 @@ import bench
 
 
 class _Rec:
+    """Issued operations with their vector clocks."""
+
     def __init__(self):
-        self.ops = []           # (kind, stream, payload) in issue order
+        self.ops = []           # (kind, stream, reads, writes, clock)
+        self.clocks = {}        # stream -> vector clock (dict stream -> count)
         self.current = None     # stream of the innermost torch.cuda.stream context
+
+    def _vc(self, stream):
+        return self.clocks.setdefault(stream, {})
+
+    def op(self, kind, stream, reads=(), writes=()):
+        vc = self._vc(stream)
+        vc[stream] = vc.get(stream, 0) + 1
+        self.ops.append((kind, stream, frozenset(reads), frozenset(writes), dict(vc)))
+
+    def record(self, stream):
+        self.op("record", stream)
+        return dict(self._vc(stream))
+
+    def wait(self, stream, snapshot):
+        vc = self._vc(stream)
+        for s, c in snapshot.items():
+            vc[s] = max(vc.get(s, 0), c)
+        self.op("wait", stream)
+
+
+def _happens_before(a, b):
+    """a's own tick on its stream is visible in b's clock."""
+    return a[4][a[1]] <= b[4].get(a[1], 0)
 
 
 def _install(monkeypatch, rec):
     class Event:
-        count = 0
-
         def __init__(self, enable_timing=False):
-            Event.count += 1
-            self.id = Event.count
+            self.snapshot = None
             self.at = None
 
         def record(self, stream=None):
+            name = getattr(stream, "name", "default")
+            self.snapshot = rec.record(name)
             self.at = len(rec.ops)
-            rec.ops.append(("record", getattr(stream, "name", "default"), self.id))
 
         def elapsed_time(self, other):
             return float(other.at - self.at)
@@ -40,7 +71,7 @@ def _install(monkeypatch, rec):
             self.name = f"s{Stream.count}"
 
         def wait_event(self, ev):
-            rec.ops.append(("wait", self.name, ev.id))
+            rec.wait(self.name, ev.snapshot)
 
     class StreamCtx:
         def __init__(self, s):
@@ -62,98 +93,138 @@ def _install(monkeypatch, rec):
         return real_empty(*a, **kw)
 
     monkeypatch.setattr(bench.torch, "empty", empty)
+    real_copy = torch.Tensor.copy_
+
+    def copy_(self, src, non_blocking=False):
+        rec.op("copy", rec.current or "default", reads={id(src)}, writes={id(self)})
+        return real_copy(self, src)
+
+    monkeypatch.setattr(torch.Tensor, "copy_", copy_)
 
 
 class _Lib:
+    """The library calls end_to_end makes, recorded with what they read and write."""
+
     def __init__(self, rec):
         self.rec = rec
 
-    def layer_fwd(self, dims, Q, K, V, qI, kI, w, o, lse, idx, kpool, ws, stream=None, o_acc=None):
-        self.rec.ops.append(("fwd", getattr(stream, "name", "default"), id(o)))
+    def _op(self, kind, stream, reads, writes):
+        self.rec.op(kind, getattr(stream, "name", "default"), {id(t) for t in reads if t is not None},
+                    {id(t) for t in writes if t is not None})
 
-    def layer_bwd(self, dims, Q, K, V, idx, o, lse, dO, dq, dk, dv, ws, stream=None, o_acc=None):
-        self.rec.ops.append(("bwd", getattr(stream, "name", "default"), id(dq)))
+    def pool_keys(self, dims, k_I, kpool, stream=None):
+        self._op("pool", stream, [k_I], [kpool])
+
+    def indexer_topk(self, dims, q_I, kpool, w, q0, n, idx, ws, ws_bytes=None, stream=None):
+        self._op("select", stream, [q_I, kpool, w], [idx, ws])
+
+    def sparse_attn_fwd(self, dims, Q, K, V, idx, o, lse, stream=None, o_acc=None):
+        self._op("fwd", stream, [Q, K, V, idx], [o, lse, o_acc])
+
+    def layer_bwd(self, dims, Q, K, V, idx, o, lse, dO, dq, dk, dv, ws=None, ws_bytes=None, stream=None,
+                  o_acc=None):
+        self._op("bwd", stream, [Q, K, V, idx, lse, dO, o_acc, ws], [dq, dk, dv])
+
+    def sparse_attn_bwd_det(self, dims, Q, K, V, idx, o, lse, dO, dq, dk, dv, ws, ws_bytes=None, stream=None,
+                            o_acc=None):
+        self._op("bwd", stream, [Q, K, V, idx, lse, dO, o_acc], [dq, dk, dv, ws])
 
 
-@pytest.mark.parametrize("with_bwd", [True, False])
-@pytest.mark.parametrize("steps", [1, 2, 5])
-def test_pipelined_schedule_orders_every_buffer_reuse(monkeypatch, with_bwd, steps):
+def _run(monkeypatch, with_bwd, steps, det=False, q_chunk=400):
     rec = _Rec()
     _install(monkeypatch, rec)
     names = ["Q", "K", "V", "q_I", "k_I", "w"] + (["dO"] if with_bwd else [])
     host = {n: torch.randn(4, 3) for n in names}
     d_in = {n: torch.zeros(4, 3) for n in names}
-    bufs = types.SimpleNamespace(o=torch.zeros(4, 3), lse=torch.zeros(4), idx=None, kpool=None, ws=None, o_acc=None)
+    bufs = types.SimpleNamespace(o=torch.zeros(4, 3), lse=torch.zeros(4), idx=torch.zeros(5), kpool=torch.zeros(6),
+                                 ws=torch.zeros(7), o_acc=torch.zeros(4, 3) if with_bwd else None)
     grads = (torch.zeros(4, 3), torch.zeros(4), torch.zeros(4)) if with_bwd else (None, None, None)
+    bws = torch.zeros(8) if det else None
     # the copy-rate measurement after the pipelined run is not part of the schedule
     monkeypatch.setattr(bench, "copy_bandwidth", lambda *a, **kw: {})
-    r = bench.end_to_end(_Lib(rec), None, types.SimpleNamespace(L=1000), host, d_in, bufs, *grads, None,
-                         torch.cuda.Stream(), types.SimpleNamespace(steps=steps, e2e_steps=steps), with_bwd, 1, "cpu")
+    dims = types.SimpleNamespace(q_chunk=q_chunk)
+    r = bench.end_to_end(_Lib(rec), dims, types.SimpleNamespace(L=1000), host, d_in, bufs, *grads, bws,
+                         torch.cuda.Stream(), types.SimpleNamespace(steps=steps, e2e_steps=steps), with_bwd, 1, "cpu",
+                         det=det)
+    return rec, r, host, d_in, names
+
+
+@pytest.mark.parametrize("with_bwd,det", [(True, False), (True, True), (False, False)])
+@pytest.mark.parametrize("steps", [1, 2, 3, 5])
+def test_pipelined_schedule_orders_every_conflicting_access(monkeypatch, with_bwd, det, steps):
+    rec, r, host, d_in, names = _run(monkeypatch, with_bwd, steps, det)
     assert r["mode"].startswith("pipelined")
     assert r["steps"] == steps
-    ov = r["overlap"]
-    assert set(ov) == {"layer_ms_mean", "layer_ms_max", "run_stream_wait_ms_mean", "fill_ms", "drain_ms"}
-    assert ov["layer_ms_max"] >= ov["layer_ms_mean"] > 0
-    assert (ov["run_stream_wait_ms_mean"] is None) == (steps == 1)
-    if steps > 1:
-        assert ov["run_stream_wait_ms_mean"] >= 0
     assert r["h2d_bytes_per_step"] == sum(t.numel() * t.element_size() for t in host.values())
     assert all(torch.equal(d_in[n], host[n]) for n in names)
 
-    # The three streams, identified by what is issued on them: input copies are
-    # recorded on one stream (plus the start event), layers on another, output
-    # copies on the third; on each stream the events come in step order.
-    layers = [op for op in rec.ops if op[0] == "fwd"]
-    assert len(layers) == steps
-    run_stream = layers[0][1]
-    records = [op for op in rec.ops if op[0] == "record"]
-    start = records[0]
-    by_stream = {}
-    for op in records[1:]:
-        by_stream.setdefault(op[1], []).append(op)
-    assert run_stream in by_stream and len(by_stream) == 3
-    in_stream = start[1]
-    out_stream = next(st for st in by_stream if st not in (in_stream, run_stream))
-    in_done = [op[2] for op in by_stream[in_stream]]
-    run_done = [op[2] for op in by_stream[run_stream]]
-    out_done = [op[2] for op in by_stream[out_stream]]
-    assert len(in_done) == len(run_done) == len(out_done) == steps
+    # every step runs its phases once, in order, on one stream: pool keys, the
+    # indexer + top-k per query chunk (1000 queries in chunks of 400: 3), the
+    # forward, the backward
+    kinds = [op[0] for op in rec.ops if op[0] in ("pool", "select", "fwd", "bwd")]
+    per_step = ["pool", "select", "select", "select", "fwd"] + (["bwd"] if with_bwd else [])
+    assert kinds == per_step * steps
+    assert len({op[1] for op in rec.ops if op[0] in ("pool", "select", "fwd", "bwd")}) == 1
+
+    # the two buffer sets alternate
+    fwd_writes = [op[3] for op in rec.ops if op[0] == "fwd"]
     if steps >= 3:
-        # the two buffer sets alternate
-        assert layers[0][2] != layers[1][2] and layers[0][2] == layers[2][2]
+        assert fwd_writes[0] != fwd_writes[1] and fwd_writes[0] == fwd_writes[2]
 
-    def waits_before(event_id):
-        """Waits issued on the event's stream between its previous record and this one."""
-        pos = next(i for i, op in enumerate(rec.ops) if op[0] == "record" and op[2] == event_id)
-        stream = rec.ops[pos][1]
-        out = []
-        for op in reversed(rec.ops[:pos]):
-            if op[0] == "record" and op[1] == stream:
-                break
-            if op[0] == "wait" and op[1] == stream:
-                out.append(op[2])
-        return set(out)
+    # happens-before for every conflicting pair of accesses
+    accesses = [op for op in rec.ops if op[2] or op[3]]
+    for i, a in enumerate(accesses):
+        for b in accesses[i + 1:]:
+            if (a[3] & (b[2] | b[3])) or (b[3] & a[2]):
+                assert _happens_before(a, b), (a[:2], b[:2])
 
-    for i in range(steps):
-        w_in, w_run, w_out = waits_before(in_done[i]), waits_before(run_done[i]), waits_before(out_done[i])
-        assert in_done[i] in w_run                       # the layer waits for its inputs
-        assert run_done[i] in w_out                      # the copy-out waits for the layer
-        if i >= 2:
-            assert run_done[i - 2] in w_in               # inputs of set i%2 free again
-            assert out_done[i - 2] in w_run              # outputs of set i%2 copied out
-        else:
-            assert not w_in
+    # copies in and out run on their own streams, concurrently with the phases
+    copy_streams = {op[1] for op in rec.ops if op[0] == "copy"}
+    run_stream = next(op[1] for op in rec.ops if op[0] == "fwd")
+    assert run_stream not in copy_streams and len(copy_streams) == 2
+
+    ov = r["overlap"]
+    assert set(ov) == {"layer_ms_mean", "layer_ms_max", "run_stream_wait_ms_mean", "fill_ms", "drain_ms"}
+    assert ov["layer_ms_max"] >= ov["layer_ms_mean"] > 0
+    assert ov["run_stream_wait_ms_mean"] >= 0 and ov["fill_ms"] > 0 and ov["drain_ms"] > 0
+
+
+def test_outputs_of_the_forward_leave_before_the_backward_ends(monkeypatch):
+    """O and LSE are copied out as soon as the forward is done: their copy
+    waits for the forward, not for the backward of the same step."""
+    rec, _, _, _, _ = _run(monkeypatch, True, 3)
+    fwd = [op for op in rec.ops if op[0] == "fwd"]
+    bwd = [op for op in rec.ops if op[0] == "bwd"]
+    for f, b in zip(fwd, bwd):
+        outs = [op for op in rec.ops if op[0] == "copy" and op[2] & f[3] and _happens_before(f, op)]
+        assert outs and not _happens_before(b, outs[0])
+
+
+def test_the_check_is_not_vacuous(monkeypatch):
+    """The same operations replayed without their event waits (stream order
+    only) leave conflicting accesses on different streams unordered, so the
+    happens-before check above can fail."""
+    rec, _, _, _, _ = _run(monkeypatch, True, 3)
+    replay = _Rec()
+    for kind, stream, reads, writes, _ in rec.ops:
+        if kind != "wait":
+            replay.op(kind, stream, reads, writes)
+    accesses = [op for op in replay.ops if op[2] or op[3]]
+    unordered = sum(1 for i, a in enumerate(accesses) for b in accesses[i + 1:]
+                    if ((a[3] & (b[2] | b[3])) or (b[3] & a[2])) and not _happens_before(a, b))
+    assert unordered > 0
 
 
 def test_serial_schedule_runs_every_step(monkeypatch):
     rec = _Rec()
     _install(monkeypatch, rec)
-    names = ["Q"]
     host = {"Q": torch.randn(3)}
     d_in = {"Q": torch.zeros(3)}
     calls = []
-    ms = bench._e2e_serial(host, names, d_in, [torch.zeros(2), torch.zeros(1)],
-                           lambda d, o, lse, g, s: calls.append(s.name), 3, torch.cuda.Stream(), "cpu")
-    assert len(calls) == 4                               # one warm-up step, three timed
+    phases = [(["Q"], lambda d, o, s: calls.append(("a", s.name)), []),
+              ([], lambda d, o, s: calls.append(("b", s.name)), [0, 1])]
+    ms = bench._e2e_serial(host, ["Q"], d_in, [torch.zeros(2), torch.zeros(1)], phases, 3, torch.cuda.Stream(), "cpu")
+    assert [c[0] for c in calls] == ["a", "b"] * 4         # one warm-up step, three timed
+    assert len({c[1] for c in calls}) == 1
     assert ms == 0.0 or ms > 0
     assert torch.equal(d_in["Q"], host["Q"])
