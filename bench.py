@@ -467,6 +467,30 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     outs = [bufs.o, bufs.lse] + ([dq, dk, dv] if with_bwd else [])
     d2h = sum(t.numel() * t.element_size() for t in outs)
     steps = max(1, args.e2e_steps)
+    phases = layer_phases(dsa, dims, wl, bufs, bws, with_bwd, det)
+    assert sorted(n for ph in phases for n in ph[0]) == sorted(names)
+    overlap = None
+    try:
+        ms, overlap = _e2e_pipelined(host, d_in, outs, phases, steps, dev)
+        mode = "pipelined: 3 streams, 2 device buffer sets, per-phase copies"
+    except Exception as exc:   # reported in the JSON line, never silent
+        torch.cuda.synchronize(dev)
+        ms = _e2e_serial(host, names, d_in, outs, phases, steps, stream, dev)
+        mode = f"serialised on one stream (pipelined run raised {type(exc).__name__}: {exc})"[:240]
+    value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
+    return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3), "mode": mode,
+            "overlap": overlap,
+            "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev),
+            # the runtime's hardware work queues per device (unset: the runtime's default)
+            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS")}
+
+
+def layer_phases(dsa, dims, wl, bufs, bws, with_bwd, det=False):
+    """The layer as (inputs it needs, run(d, o, stream), indices into the
+    outputs [O, LSE, dQ, dK, dV] it completes), in order: pool keys and
+    indexer + top-k per query chunk (the first part of dsa_layer_fwd), the
+    attention forward, the backward."""
     C = int(dims.q_chunk)
     chunks = [(q0, min(C, wl.L - q0)) for q0 in range(0, wl.L, C)]
 
@@ -486,26 +510,10 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
             dsa.layer_bwd(dims, d["Q"], d["K"], d["V"], bufs.idx, o[0], o[1], d["dO"], o[2], o[3], o[4], bws,
                           stream=s, o_acc=bufs.o_acc)
 
-    # (inputs the phase needs, the phase, indices into outs it completes)
     phases = [(["k_I", "q_I", "w"], select, []), (["Q", "K", "V"], forward, [0, 1])]
     if with_bwd:
         phases.append((["dO"], backward, [2, 3, 4]))
-    assert sorted(n for ph in phases for n in ph[0]) == sorted(names)
-    overlap = None
-    try:
-        ms, overlap = _e2e_pipelined(host, d_in, outs, phases, steps, dev)
-        mode = "pipelined: 3 streams, 2 device buffer sets, per-phase copies"
-    except Exception as exc:   # reported in the JSON line, never silent
-        torch.cuda.synchronize(dev)
-        ms = _e2e_serial(host, names, d_in, outs, phases, steps, stream, dev)
-        mode = f"serialised on one stream (pipelined run raised {type(exc).__name__}: {exc})"[:240]
-    value, ms, _ = aggregate_replicas(ms, wl.L * steps, world, dev)
-    return {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 3), "mode": mode,
-            "overlap": overlap,
-            "copy_bandwidth": copy_bandwidth(host, names, d_in, outs, stream, dev),
-            # the runtime's hardware work queues per device (unset: the runtime's default)
-            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS")}
+    return phases
 
 
 def copy_bandwidth(host, names, d_in, outs, stream, dev):
@@ -536,8 +544,9 @@ def copy_bandwidth(host, names, d_in, outs, stream, dev):
             "d2h_gbs": round(d2h_b / (ms_out * 1e-3) / 1e9, 1), "d2h_ms": round(ms_out, 3)}
 
 
-def _e2e_pipelined(host, d_in, outs, phases, steps, dev):
-    """Total ms of `steps` pipelined steps (see end_to_end) and where it went."""
+def _e2e_pipelined(host, d_in, outs, phases, steps, dev, sink=None):
+    """Total ms of `steps` pipelined steps (see end_to_end) and where it went.
+    sink (a list): receives the pinned host copies of the last step's outputs."""
     names = [n for ph in phases for n in ph[0]]
     sets = [(d_in, outs), ({n: torch.empty_like(d_in[n]) for n in names}, [torch.empty_like(t) for t in outs])]
     pinned = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in sets]
@@ -599,6 +608,8 @@ def _e2e_pipelined(host, d_in, outs, phases, steps, dev):
                "run_stream_wait_ms_mean": round(sum(wait_ms) / steps, 3),
                "fill_ms": round(t(in_done[0][0]), 3),
                "drain_ms": round(t(out_done[-1][last_out]) - t(ph_done[-1][-1]), 3)}
+    if sink is not None:
+        sink.append(pinned[(steps - 1) % 2])
     return t(out_done[-1][last_out]), overlap
 
 
