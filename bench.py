@@ -455,10 +455,11 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     The layer runs as its three phases, each through its own entry points:
     pool keys and indexer + top-k per query chunk (what dsa_layer_fwd does
     first), the attention forward, the backward.  Consecutive steps are
-    pipelined over three streams with two device buffer sets: a phase waits
-    only for its own inputs (k_I, q_I, w; then Q, K, V; then dO), and O and
-    LSE go back as soon as the forward is done, so the copies of one step
-    overlap the phases of its neighbours and of itself.  --e2e-steps steps (10
+    pipelined with two device buffer sets, the phases on one stream and the
+    copies on another (_e2e_pipelined): a phase waits only for its own inputs
+    (k_I, q_I, w; then Q, K, V; then dO), the next step's inputs go in while
+    this one runs, and O and LSE go back as soon as the forward is done.
+    --e2e-steps steps (10
     by default) are timed, pipeline fill and drain included, and the box's
     measured copy rates are reported beside the figure.  If the pipelined run
     raises, the serialised run is reported and "mode" says why."""
@@ -472,7 +473,7 @@ def end_to_end(dsa, dims, wl, host, d_in, bufs, dq, dk, dv, bws, stream, args, w
     overlap = None
     try:
         ms, overlap = _e2e_pipelined(host, d_in, outs, phases, steps, dev)
-        mode = "pipelined: 3 streams, 2 device buffer sets, per-phase copies"
+        mode = "pipelined: a run stream and one copy stream, 2 device buffer sets, per-phase copies"
     except Exception as exc:   # reported in the JSON line, never silent
         torch.cuda.synchronize(dev)
         ms = _e2e_serial(host, names, d_in, outs, phases, steps, stream, dev)
@@ -546,11 +547,19 @@ def copy_bandwidth(host, names, d_in, outs, stream, dev):
 
 def _e2e_pipelined(host, d_in, outs, phases, steps, dev, sink=None):
     """Total ms of `steps` pipelined steps (see end_to_end) and where it went.
-    sink (a list): receives the pinned host copies of the last step's outputs."""
+    sink (a list): receives the pinned host copies of the last step's outputs.
+
+    Two streams: the layer's phases run on one, every copy on the other, in
+    the order the copies are needed.  When step i starts (its buffer set's
+    previous user, step i-2, is done, and so is step i-1, the other set's) the
+    inputs of step i+1 go in; O and LSE of step i go out when its forward is
+    done, its gradients when its backward is done.  So copies never run at the
+    same time as one another -- concurrent copies in both directions slowed
+    each other several-fold on some boxes -- while each overlaps the kernels."""
     names = [n for ph in phases for n in ph[0]]
     sets = [(d_in, outs), ({n: torch.empty_like(d_in[n]) for n in names}, [torch.empty_like(t) for t in outs])]
     pinned = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in sets]
-    s_in, s_run, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_run, s_cp = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     P = len(phases)
 
     def ev():
@@ -559,30 +568,47 @@ def _e2e_pipelined(host, d_in, outs, phases, steps, dev, sink=None):
     in_done = [[ev() for _ in range(P)] for _ in range(steps)]     # a phase's inputs are in
     ph_done = [[ev() for _ in range(P)] for _ in range(steps)]     # a phase has run
     out_done = [[ev() for _ in range(P)] for _ in range(steps)]    # a phase's outputs are out
-    torch.cuda.synchronize(dev)
-    start = ev()
-    start.record(s_in)
-    for i in range(steps):
-        d, o = sets[i % 2]
-        if i >= 2:
-            s_in.wait_event(ph_done[i - 2][-1])   # step i-2 has finished reading this input set
+
+    def copy_in(i):
+        d = sets[i % 2][0]
         for p, (inputs, _, _) in enumerate(phases):
-            with torch.cuda.stream(s_in):
+            with torch.cuda.stream(s_cp):
                 for n in inputs:
                     d[n].copy_(host[n], non_blocking=True)
-            in_done[i][p].record(s_in)
+            in_done[i][p].record(s_cp)
+
+    # one untimed pass of every copy over every buffer: freshly allocated
+    # pinned memory is slow on its first transfers
+    with torch.cuda.stream(s_cp):
+        for d, o in sets:
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+        for k in range(len(sets)):
+            for src, dst in zip(outs, pinned[k]):
+                dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    start = ev()
+    start.record(s_cp)
+    copy_in(0)
+    for i in range(steps):
+        d, o = sets[i % 2]
         for p, (_, run, outputs) in enumerate(phases):
             s_run.wait_event(in_done[i][p])
             if i >= 2 and outputs:
                 s_run.wait_event(out_done[i - 2][p])   # step i-2's outputs in this set have been copied out
             run(d, o, s_run)
             ph_done[i][p].record(s_run)
+        if i + 1 < steps:
+            if i >= 1:
+                s_cp.wait_event(ph_done[i - 1][-1])    # step i-1 has finished reading the next step's set
+            copy_in(i + 1)
+        for p, (_, _, outputs) in enumerate(phases):
             if outputs:
-                s_out.wait_event(ph_done[i][p])
-                with torch.cuda.stream(s_out):
+                s_cp.wait_event(ph_done[i][p])
+                with torch.cuda.stream(s_cp):
                     for j in outputs:
                         pinned[i % 2][j].copy_(o[j], non_blocking=True)
-                out_done[i][p].record(s_out)
+                out_done[i][p].record(s_cp)
     torch.cuda.synchronize(dev)
     # Where the time went, from the same events: a phase can begin once its
     # inputs are in, its buffer set's previous outputs are out and the phase

@@ -2,8 +2,8 @@
 streams and events.
 
 The pipelined schedule runs each step's three phases (indexer + top-k, the
-forward, the backward) on one stream, the input copies on a second and the
-output copies on a third, over two device buffer sets.  The stand-ins record
+forward, the backward) on one stream and every copy on a second, over two
+device buffer sets.  The stand-ins record
 every copy and every library call with the buffers it reads and writes, and
 vector clocks give the happens-before order that stream order and event
 waits establish.  The check: every two accesses to one buffer, at least one
@@ -178,10 +178,19 @@ def test_pipelined_schedule_orders_every_conflicting_access(monkeypatch, with_bw
             if (a[3] & (b[2] | b[3])) or (b[3] & a[2]):
                 assert _happens_before(a, b), (a[:2], b[:2])
 
-    # copies in and out run on their own streams, concurrently with the phases
+    # copies in and out share one stream of their own, apart from the phases,
+    # so two copies never run at once
     copy_streams = {op[1] for op in rec.ops if op[0] == "copy"}
     run_stream = next(op[1] for op in rec.ops if op[0] == "fwd")
-    assert run_stream not in copy_streams and len(copy_streams) == 2
+    assert run_stream not in copy_streams and len(copy_streams) == 1
+
+    # the next step's inputs are queued before this step's outputs
+    copies = [op for op in rec.ops if op[0] == "copy"]
+    if steps >= 2:
+        host_ids = {id(t) for t in host.values()}
+        h2d = [k for k, op in enumerate(copies) if op[2] & host_ids]
+        first_out = next(k for k, op in enumerate(copies) if op[2] & fwd_writes[0])
+        assert all(k < first_out for k in h2d[len(names):2 * len(names)])
 
     ov = r["overlap"]
     assert set(ov) == {"layer_ms_mean", "layer_ms_max", "run_stream_wait_ms_mean", "fill_ms", "drain_ms"}
