@@ -65,8 +65,8 @@ TRAFFIC = {
     ("bf16_128k_needle", "attn_fwd"): {"bytes": 1271921920 + 1564575744,
                                        "sources": {"attn_fwd.cu": "ffdff854d43dc7cb", "gather.cuh": "9c5588b13d0916cd", "common.cuh": "4c65dfd5da7caf78"}},
     # mean over the 16 chunk launches of one step
-    ("bf16_128k_needle", "indexer"): {"bytes": 37685632 + 480333056,
-                                      "sources": {"indexer_tc.cu": "6267c910c1505ced", "common.cuh": "4c65dfd5da7caf78"}},
+    ("bf16_128k_needle", "indexer"): {"bytes": 36841456 + 477152544,
+                                      "sources": {"indexer_tc.cu": "4152b6e7fe6b5292", "common.cuh": "4c65dfd5da7caf78"}},
     ("bf16_128k_needle", "topk"): {"bytes": 538500512 + 11403616,
                                    "sources": {"topk.cu": "7e34eb4699bcd34b", "common.cuh": "4c65dfd5da7caf78"}},
 }

@@ -8,13 +8,16 @@
 //   s[t,p] = sum_h w[t,h] * max(0, q_I[t,h,:] . kpool[p,:]),   p < elig(t).
 //
 // Design (one persistent CTA per SM, warp-specialised):
-//   * MMA shape M=128 pools x N=32*Hi x K=16.  The Hi heads of a 32-query
-//     block are Hi*32 consecutive rows of q_I ([L, Hi, di] row-major), so one
-//     MMA computes D[p, t*Hi+h] = kpool[p,:] . q_I[t,h,:] for all heads at
-//     once (N = 256 at Hi = 8), with fp32 accumulators in tensor memory.  An
-//     epilogue thread owns one pool (TMEM lane) and finds the Hi heads of a
-//     query in adjacent columns of its own registers, so ReLU, the head weight
-//     and the head sum need no cross-thread exchange.
+//   * MMA shape M=128 pools x N=32*Hi x K=16.  A 3D TMA box loads the q_I
+//     rows of a 32-query block ([L, Hi, di] row-major) head-major into shared
+//     memory (row h*32 + t), so one MMA computes D[p, h*32+t] = kpool[p,:] .
+//     q_I[t,h,:] for all heads at once (N = 256 at Hi = 8), with fp32
+//     accumulators in tensor memory.  An epilogue thread owns one pool (TMEM
+//     lane) and holds every head of its queries in its own registers, so
+//     ReLU, the head weight and the head sum need no cross-thread exchange;
+//     head-major columns put consecutive queries of one head side by side, so
+//     the weighted sums of two queries advance in one packed fp32x2 FMA (each
+//     query's FMA chain over the heads is unchanged: the same bits).
 //   * Two accumulators (2 x Hi x 32 columns) let the MMAs of tile i+1 run
 //     while the epilogue drains tile i.
 //   * Warp 0 issues TMA loads (128-byte swizzle): the q_I block of a work unit
@@ -69,6 +72,25 @@ struct IdxCfg {
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
+
+// A 3D TMA tile load signalling `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];\n" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// Eight consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 // One-lane operations of the epilogue as predicated instructions (no branch
 // and no reconvergence around them): the lane with `pred` set performs them.
@@ -211,7 +233,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         if (!(ok = mbar_wait(empty_b(bb), ((b_iter >> 1) & 1) ^ 1, abort_flag))) break;
         mbar_arrive_expect_tx(full_b(bb), C::B_BYTES);
         for (int c = 0; c < C::KC; ++c)
-          tma_load_2d(sB + bb * C::B_BYTES + c * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, (int32_t)(it.t0 * HI));
+          tma_load_3d(sB + bb * C::B_BYTES + c * C::B_CHUNK, &tmap_q, full_b(bb), 64 * c, (int32_t)it.t0, 0);
         ++b_iter;
         for (int tile = it.tile_begin; tile < it.tile_end; ++tile) {
           const int s = a_iter % C::NSA;
@@ -278,7 +300,7 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     const int lane_base = quarter * 32;
     uint32_t acc_iter = 0;
     bool ok = true;
-    float* w_mine = w_s + ew * C::QPW * HI;  // this warp's QPW queries x HI weights
+    float* w_mine = w_s + ew * C::QPW * HI;  // this warp's HI heads x QPW queries (head-major)
     // emit mode, per query of this warp (8 words): [0] tau, [4] sub-list
     // capacity, [5..6] sub-list base (64-bit), [7] sub-list length so far
     // (words 4..7 are read as one 16-byte vector).  The lengths live in
@@ -288,12 +310,12 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
     const uint32_t emit_sa = smem_u32(emit_mine);
     const uint32_t w_mine_s = smem_u32(w_mine);
     uint32_t stg_iter = 0;
-    constexpr int NLD = C::QPW * HI / 16;    // 16-column TMEM loads per tile
+    static_assert(C::QPW == 8, "a warp's queries of one head are one 8-column TMEM load");
     while (ok && it.next<C::BN, C::BM, C::SEG>()) {
       __syncwarp();
       for (int i = lane; i < C::QPW * HI; i += 32) {
-        const int64_t t = it.t0 + qg * C::QPW + i / HI;
-        w_mine[i] = t < q_end ? __ldg(w + t * HI + (i % HI)) : 0.f;
+        const int64_t t = it.t0 + qg * C::QPW + i % C::QPW;
+        w_mine[i] = t < q_end ? __ldg(w + t * HI + i / C::QPW) : 0.f;
       }
       // emit mode: the threshold and this warp's sub-list of each of its
       // queries for this unit (segment seg, lane quarter `quarter`); +inf and
@@ -324,31 +346,40 @@ __global__ void __launch_bounds__(IdxCfg<HI, DI>::THREADS, 1)
         const int ab = acc_iter & 1;
         if (!(ok = mbar_wait(tfull(ab), (acc_iter >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        // this thread: pool (lane_base + lane), queries qg*QPW .. +QPW-1, columns
-        // (query*Hi + head) -- all loaded before one wait
-        const uint32_t taddr =
-            tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + qg * C::QPW * HI;
-        float v[NLD][16];
+        // this thread: pool (lane_base + lane), queries qg*QPW .. +QPW-1 of head
+        // h in columns h*BN + qg*QPW .. +QPW-1 -- all loaded before one wait
+        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + ab * C::ACC_COLS + qg * C::QPW;
+        float v[HI][C::QPW];
 #pragma unroll
-        for (int i = 0; i < NLD; ++i) tmem_ld16(taddr + i * 16, v[i]);
+        for (int h = 0; h < HI; ++h) tmem_ld8(taddr + h * C::BN, v[h]);
         tmem_ld_wait();
         // the accumulator is in registers: hand it back to the MMA warp
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(tempty(ab), lane == 0);
         const int64_t p = (int64_t)tile * C::BM + lane_base + lane;
+        // acc[j] = fma(relu(s_h), w_h, acc[j]) over heads h = 0..Hi-1 in order,
+        // two queries per packed FMA
+        float2 acc2[C::QPW / 2];
+#pragma unroll
+        for (int jp = 0; jp < C::QPW / 2; ++jp) acc2[jp] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int h = 0; h < HI; ++h) {
+          // weights of head h for the warp's queries (broadcast, explicit shared loads)
+          const float4 wa = ld_shared_v4(w_mine_s + 4 * (h * C::QPW));
+          const float4 wb = ld_shared_v4(w_mine_s + 4 * (h * C::QPW + 4));
+          const float2 w2[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w), make_float2(wb.x, wb.y),
+                                make_float2(wb.z, wb.w)};
+#pragma unroll
+          for (int jp = 0; jp < C::QPW / 2; ++jp)
+            acc2[jp] = __ffma2_rn(make_float2(fmaxf(v[h][2 * jp], 0.f), fmaxf(v[h][2 * jp + 1], 0.f)), w2[jp],
+                                  acc2[jp]);
+        }
         float acc[C::QPW];
 #pragma unroll
-        for (int j = 0; j < C::QPW; ++j) acc[j] = 0.f;
-#pragma unroll
-        for (int c4 = 0; c4 < NLD * 4; ++c4) {
-          const float4 q4 = ld_shared_v4(w_mine_s + 16 * c4);   // broadcast (explicit shared load)
-          const float wq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;            // heads of one query in order 0..Hi-1
-            acc[c / HI] = fmaf(fmaxf(v[c / 16][c % 16], 0.f), wq[e], acc[c / HI]);
-          }
+        for (int jp = 0; jp < C::QPW / 2; ++jp) {
+          acc[2 * jp] = acc2[jp].x;
+          acc[2 * jp + 1] = acc2[jp].y;
         }
         if constexpr (EMIT) {
           // candidates: every eligible score >= the row's threshold goes to
@@ -457,11 +488,13 @@ static cudaError_t launch_tc(int64_t L, const void* q_idx, const void* kpool, Id
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tq, tk;
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)L * HI};
-    const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)C::NCOL};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_idx), dims, strides, box, estr,
+    // q_I [L, Hi, di] seen as (di, t, h): a box of 32 queries x Hi heads lands
+    // head-major in shared memory (row h*32 + t)
+    const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)L, (cuuint64_t)HI};
+    const cuuint64_t strides[2] = {(cuuint64_t)HI * DI * 2, (cuuint64_t)DI * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)C::BN, (cuuint32_t)HI};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
