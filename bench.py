@@ -785,7 +785,8 @@ def main():
     ap.add_argument("--workload", default="bf16_128k_needle", choices=sorted(dsa_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=24, help="oracle rows per reference step")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="oracle rows for the cpu_baseline field")
+    ap.add_argument("--cpu-rows", type=int, default=384,
+                    help="oracle rows for the cpu_baseline field (384: about 10 s of one host core at 128k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10, help="end-to-end steps (at least 1; 10 by default)")
     ap.add_argument("--indexer-route", type=int, default=1, choices=[0, 1],
