@@ -14,7 +14,8 @@
 * integer twins of the 128k-needle and 256k workloads: the selection bit for
   bit on sampled rows of 32768 and 65536 pools;
 * the tcgen05 forward (route 1) at full size against the warp-level forward on
-  every row and against the oracle on sampled rows.
+  every row and against the oracle on sampled rows;
+* the two indexer + top-k routes against each other over every row at full size.
 """
 import math
 import os
@@ -328,3 +329,35 @@ def test_full_size_tcgen05_forward(name):
     assert np.abs(_f32(o1)[rows] - O).max() <= 2e-2
     assert np.abs(a1.cpu().numpy()[rows] - O).max() <= 1e-4
     assert np.abs(l1.cpu().numpy()[rows] - LSE).max() <= 1e-3
+
+
+@pytest.mark.parametrize("name", ["bf16_128k_needle", "bf16_1m_ties"])
+def test_full_size_indexer_routes_agree(name):
+    """The two indexer + top-k routes of dsa_indexer_topk select the same pools
+    bit for bit over every row of a full-size workload: route 1 (the score
+    block and the row-wise top-k, checked against the oracle on sampled rows
+    above) and route 0 (candidate lists, no score block).  At 1M the integer
+    indexer inputs make thousands of exact ties per row, which overflow route
+    0's candidate lists and send rows through its fallback."""
+    wl = dsa_inputs.WORKLOADS[name]
+    host = dsa_inputs.make(wl, ("q_I", "k_I", "w"))
+    dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, scale=wl.scale, dtype=wl.dtype)
+    dev = {n: t.to(DEV) for n, t in host.items()}
+    kpool = torch.empty((wl.L // 4, wl.di), dtype=dev["k_I"].dtype, device=DEV)
+    dsa.pool_keys(dims, dev["k_I"], kpool)
+    ws = torch.empty(dsa.indexer_topk_workspace_bytes(dims, wl.q_chunk), dtype=torch.uint8, device=DEV)
+    out = {}
+    try:
+        for route in (1, 0):
+            dsa.set_indexer_topk_route(route)
+            idx = torch.full((wl.L, wl.k), -7, dtype=torch.int32, device=DEV)
+            for q0 in range(0, wl.L, wl.q_chunk):
+                n = min(wl.q_chunk, wl.L - q0)
+                dsa.indexer_topk(dims, dev["q_I"], kpool, dev["w"], q0, n, idx, ws)
+            dsa.check_device_error()
+            out[route] = idx
+    finally:
+        dsa.set_indexer_topk_route(1)
+    same = (out[0] == out[1]).all(dim=1)
+    assert bool(same.all()), torch.nonzero(~same)[:5].flatten().tolist()
+    assert int((out[1] == -7).sum()) == 0
