@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import dsa_inputs
 import oracle
 import long_context_sparse_dsa_gb300 as dsa
 
@@ -121,6 +122,28 @@ def test_pool_keys_gated_bitexact(dtype, di):
     dsa.pool_keys(dims, k_I.to(DEV), kp0)
     dsa.check_device_error()
     assert torch.equal(kp1.view(torch.uint8), kp0.view(torch.uint8))
+
+
+@pytest.mark.parametrize("name", ["bf16_128k_needle", "bf16_1m_ties"])
+def test_pool_keys_full_size_bitexact(name):
+    """Plain and gated pool keys of a full-size workload's own k_I, every pool,
+    against the oracle bit for bit (gates of both signs, zeros and assorted
+    magnitudes)."""
+    wl = dsa_inputs.WORKLOADS[name]
+    k_I = dsa_inputs.make(wl, ("k_I",))["k_I"]
+    g = torch.Generator().manual_seed(33)
+    gate = torch.randn(wl.L, generator=g) * torch.exp2(torch.randint(-6, 7, (wl.L,), generator=g).float())
+    gate[::17] = 0.0
+    dims = dsa.make_dims(wl.L, wl.Hq, wl.d, wl.Hi, wl.di, wl.k, q_chunk=wl.q_chunk, dtype=wl.dtype)
+    kp = torch.empty((wl.L // 4, wl.di), dtype=torch.bfloat16, device=DEV)
+    kg = torch.empty_like(kp)
+    kd = k_I.to(DEV)
+    dsa.pool_keys(dims, kd, kp)
+    dsa.pool_keys_gated(dims, kd, gate.to(DEV), kg)
+    dsa.check_device_error()
+    kf = _f32(k_I)
+    assert np.array_equal(_f32(kp).view(np.uint32), oracle.pool_keys(kf, True).view(np.uint32))
+    assert np.array_equal(_f32(kg).view(np.uint32), oracle.pool_keys_gated(kf, gate.numpy(), True).view(np.uint32))
 
 
 def test_gated_pools_feed_the_selection_bitexact():
