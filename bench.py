@@ -550,12 +550,12 @@ def _e2e_pipelined(host, d_in, outs, phases, steps, dev, sink=None):
     sink (a list): receives the pinned host copies of the last step's outputs.
 
     Two streams: the layer's phases run on one, every copy on the other, in
-    the order the copies are needed.  When step i starts (its buffer set's
-    previous user, step i-2, is done, and so is step i-1, the other set's) the
-    inputs of step i+1 go in; O and LSE of step i go out when its forward is
-    done, its gradients when its backward is done.  So copies never run at the
-    same time as one another -- concurrent copies in both directions slowed
-    each other several-fold on some boxes -- while each overlaps the kernels."""
+    the order the copies are needed.  When step i starts, step i-1 -- the last
+    user of the other buffer set -- is done, so the inputs of step i+1 go into
+    that set; O and LSE of step i go out when its forward is done, its
+    gradients when its backward is done.  So copies never run at the same time
+    as one another -- concurrent copies in both directions slowed each other
+    several-fold on some boxes -- while each overlaps the kernels."""
     names = [n for ph in phases for n in ph[0]]
     sets = [(d_in, outs), ({n: torch.empty_like(d_in[n]) for n in names}, [torch.empty_like(t) for t in outs])]
     pinned = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in sets]
